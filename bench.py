@@ -1,0 +1,396 @@
+"""Benchmark of the exact-attention hot path on GB300.
+
+One step = one pass over every stage of the path on one synthetic batch:
+  * prefill: fused attention forward on the Llama-3-8B-shaped workload
+    (B=2, H=32, N=4096, d=128, causal, bf16), stages a1-a7;
+  * decode: Flash-Decoding split + merge on B=16, H=32, L=32768, d=128
+    (bf16 KV cache of 8.6 GB), stages a8-a9.
+The headline ``value`` is the prefill's TFLOP/s (matmul FLOPs 4 B H N^2 d,
+halved for causal, over the summed device time of the prefill launches);
+the decode's KV-read GB/s is reported beside it under ``decode``.
+
+Prints one JSON line (rank 0). ``--impl reference`` times the fp64 CPU
+oracle on a bounded sample of the same workload instead.
+
+Multi-GPU (torchrun, one rank per GPU): every rank runs its own batch (weak
+scaling, no collective on the data path); value = all ranks' FLOPs over the
+max time across ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "attn fwd TFLOP/s (% of GB300 BF16 peak); decode KV-read GB/s (% of HBM)"
+PREFILL_NAME = "llama3_8b_prefill"
+DECODE_NAME = "decode_32k"
+DEFAULT_SPLITS = 16
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+FALLBACK_BF16_TFLOPS_SUSTAINED = 1700.0
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": float(p["hbm_gbs"]), "bf16_tflops": float(p["bf16_tflops"]),
+                "bf16_tflops_sustained": float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                "source": "measured"}
+    return {"hbm_gbs": FALLBACK_HBM_GBS, "bf16_tflops": FALLBACK_BF16_TFLOPS,
+            "bf16_tflops_sustained": FALLBACK_BF16_TFLOPS_SUSTAINED, "source": "fallback"}
+
+
+def _profile_traffic():
+    """DRAM bytes per launch from the committed ncu summary, keyed by kernel tag."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.md")
+    out = {}
+    if not os.path.exists(path):
+        return out
+    for line in open(path):
+        parts = [p.strip() for p in line.strip().strip("|").split("|")]
+        if len(parts) >= 4 and parts[0].startswith("traffic:"):
+            try:
+                out[parts[0][len("traffic:"):]] = float(parts[3])
+            except ValueError:
+                pass
+    return out
+
+
+class ClockSampler:
+    """Samples SM clocks, power and throttle reasons with nvidia-smi while running."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.lines = []
+        self.t0 = self.t1 = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.gpu_id, f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+            return
+        self._reader = threading.Thread(target=self._read, daemon=True)
+        self._reader.start()
+        time.sleep(0.3)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def mark(self, which):
+        if which == "start":
+            self.t0 = time.time()
+        else:
+            self.t1 = time.time()
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        for ts, line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            rows.append((ts, parts))
+        inside = [r for ts, r in rows if self.t0 is not None and self.t0 - 0.06 <= ts <= (self.t1 or ts) + 0.06]
+        if not inside and rows:  # timed region shorter than the sampling period: nearest samples
+            mid = (self.t0 + self.t1) / 2 if self.t0 and self.t1 else rows[-1][0]
+            inside = [min(rows, key=lambda r: abs(r[0] - mid))[1]]
+        if not inside:
+            return None
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+
+        sm = [num(r[0]) for r in inside if num(r[0]) is not None]
+        smax = [num(r[1]) for r in inside if num(r[1]) is not None]
+        reasons = set()
+        for r in inside:
+            for name, val in zip(("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"),
+                                 r[4:8]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(inside)}
+
+
+def _dist():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def reduce_max(values, world):
+    """Element-wise max of a list of floats over all ranks (no-op when world == 1)."""
+    if world == 1:
+        return list(values)
+    import torch
+    import torch.distributed as dist
+
+    backend = dist.get_backend()
+    dev = "cuda" if backend == "nccl" else "cpu"
+    t = torch.tensor(values, dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.cpu().tolist()
+
+
+def _cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def cpu_oracle_sample(n_heads: int, seed: int = 0):
+    """Time the fp64 oracle on the first n_heads (b, h) of the prefill workload
+    (every row of each head); returns (tflops, seconds, flops, description)."""
+    import numpy as np
+
+    import oracle
+    from exact_attention_29_gb300 import perfmodel
+    from exact_attention_29_gb300 import workloads as wl
+
+    c = wl.PREFILL[PREFILL_NAME]
+    q, k, v = wl.prefill_inputs(c.B, c.H, c.N, c.d, seed=seed)
+    heads = [(b, h) for b in range(c.B) for h in range(c.H)][:n_heads]
+    qs = [(q[b, h].double().numpy(), k[b, h].double().numpy(), v[b, h].double().numpy()) for b, h in heads]
+    oracle.build()
+    pos = np.arange(c.N)
+    t0 = time.perf_counter()
+    for qq, kk, vv in qs:
+        oracle.attention_rows(qq, pos, kk, vv, c.causal, c.scale)
+    dt = time.perf_counter() - t0
+    flops = perfmodel.fwd_flops(1, len(heads), c.N, c.d, c.causal)
+    return flops / dt / 1e12, dt, flops, f"{len(heads)} of {c.B * c.H} heads of {PREFILL_NAME}, all {c.N} rows each"
+
+
+def run_reference(args, world, rank):
+    """The reference arm: the fp64 CPU oracle, as it stands, on the host cores."""
+    if rank != 0:
+        return
+    heads = 2
+    for _ in range(args.warmup):
+        cpu_oracle_sample(1)
+    times, flops_total = [], 0.0
+    desc = ""
+    for _ in range(args.steps):
+        _, dt, fl, desc = cpu_oracle_sample(heads)
+        times.append(dt)
+        flops_total += fl
+    total = sum(times)
+    value = flops_total / total / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / max(1, args.steps),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": PREFILL_NAME, "B": 2, "H": 32, "N": 4096, "d": 128, "causal": True,
+                   "sample_per_step": desc},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": _cores(), "kind": "oracle", "sample": desc},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_gpu(args, world, rank, local):
+    import torch
+
+    import exact_attention_29_gb300 as fa
+    from exact_attention_29_gb300 import build as fa_build
+    from exact_attention_29_gb300 import perfmodel
+    from exact_attention_29_gb300 import workloads as wl
+
+    fa_build.build()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=dev)
+
+    pc = wl.PREFILL[PREFILL_NAME]
+    dc = wl.DECODE[DECODE_NAME]
+    splits = args.splits
+    q, k, v = wl.prefill_inputs(pc.B, pc.H, pc.N, pc.d, seed=rank, device=dev)
+    o = torch.empty_like(q)
+    lse = torch.empty((pc.B, pc.H, pc.N), dtype=torch.float32, device=dev)
+    dq, kc, vc, seqlens = wl.decode_inputs(dc.B, dc.H, dc.L, dc.d, seed=rank, device=dev)
+    do_ = torch.empty_like(dq)
+    dlse = torch.empty((dc.B, dc.H), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(evs=None):
+        if evs is not None:
+            evs[0].record(stream)
+        fa.fa_fwd(q, k, v, causal=pc.causal, o=o, lse=lse, stream=stream)
+        if evs is not None:
+            evs[1].record(stream)
+        fa.fa_decode(dq, kc, vc, seqlens, splits, o=do_, lse=dlse, stream=stream)
+        if evs is not None:
+            evs[2].record(stream)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    fa.fa_check_device_error(stream)
+    torch.cuda.synchronize(dev)
+
+    props = torch.cuda.get_device_properties(dev)
+    gpu_id = str(getattr(props, "uuid", local))
+    if gpu_id and not gpu_id.startswith("GPU-") and len(gpu_id) > 8:
+        gpu_id = "GPU-" + gpu_id
+    sampler = ClockSampler(gpu_id)
+    if rank == 0:
+        sampler.start()
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    sampler.mark("start")
+    t_start.record(stream)
+    for i in range(args.steps):
+        step(evs[i])
+    t_end.record(stream)
+    torch.cuda.synchronize(dev)
+    sampler.mark("end")
+    if world > 1:
+        dist.barrier()
+    clocks = sampler.stop() if rank == 0 else None
+    fa.fa_check_device_error(stream)
+
+    total_ms = t_start.elapsed_time(t_end)
+    fwd_ms = sum(e[0].elapsed_time(e[1]) for e in evs)
+    dec_ms = sum(e[1].elapsed_time(e[2]) for e in evs)
+    total_ms, fwd_ms, dec_ms = reduce_max([total_ms, fwd_ms, dec_ms], world)
+
+    fwd_flops = perfmodel.fwd_flops(pc.B, pc.H, pc.N, pc.d, pc.causal)
+    kv_bytes = perfmodel.decode_kv_bytes(dc.H, dc.d, seqlens.tolist())
+    dec_bytes = perfmodel.decode_algorithmic_bytes(dc.B, dc.H, dc.d, seqlens.tolist())
+    value = world * fwd_flops * args.steps / (fwd_ms * 1e-3) / 1e12
+    dec_gbs = world * kv_bytes * args.steps / (dec_ms * 1e-3) / 1e9
+
+    # end to end through the public API with pinned host buffers: H2D of q/k/v,
+    # the C-ABI call, D2H of o and lse, all inside the timed region
+    hq, hk, hv = (t.cpu().pin_memory() for t in (q, k, v))
+    ho = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+    hl = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    e2e_steps = max(1, min(args.steps, 10))
+
+    def e2e_step():
+        q.copy_(hq, non_blocking=True)
+        k.copy_(hk, non_blocking=True)
+        v.copy_(hv, non_blocking=True)
+        fa.fa_fwd(q, k, v, causal=pc.causal, o=o, lse=lse, stream=stream)
+        ho.copy_(o, non_blocking=True)
+        hl.copy_(lse, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize(dev)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = reduce_max([e0.elapsed_time(e1)], world)[0]
+    e2e_value = world * fwd_flops * e2e_steps / (e2e_ms * 1e-3) / 1e12
+    h2d = sum(t.numel() * t.element_size() for t in (q, k, v))
+    d2h = o.numel() * o.element_size() + lse.numel() * lse.element_size()
+
+    if rank != 0:
+        return
+    peaks = _peaks()
+    long_region = total_ms > 1000.0
+    tflops_peak = peaks["bf16_tflops_sustained"] if long_region else peaks["bf16_tflops"]
+    tag = "of measured" if peaks["source"] == "measured" else "of fallback"
+    traffic = _profile_traffic()
+    fwd_avg_ms = fwd_ms / args.steps
+    dec_avg_ms = dec_ms / args.steps
+    fwd_roof = {"bound": "tensor", "achieved": fwd_flops / (fwd_avg_ms * 1e-3) / 1e12, "peak": tflops_peak,
+                "unit": "TFLOP/s", "traffic": traffic.get("fwd_kernel_128_llama3_8b_prefill"),
+                "kernel": "fwd_kernel<128>", "peak_kind": ("sustained " if long_region else "burst ") + tag}
+    fwd_roof["frac"] = fwd_roof["achieved"] / fwd_roof["peak"]
+    dec_roof = {"bound": "hbm", "achieved": dec_bytes / (dec_avg_ms * 1e-3) / 1e9, "peak": peaks["hbm_gbs"],
+                "unit": "GB/s", "traffic": traffic.get("decode_split_kernel_128_decode_32k"),
+                "kernel": "decode_split_kernel<128> + decode_merge_kernel<128>", "peak_kind": "copy " + tag}
+    dec_roof["frac"] = dec_roof["achieved"] / dec_roof["peak"]
+    dominant = dec_roof if dec_avg_ms >= fwd_avg_ms else fwd_roof
+
+    c_tflops, c_dt, _, c_desc = cpu_oracle_sample(args.cpu_heads)
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": max(3, args.warmup), "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"{PREFILL_NAME} + {DECODE_NAME}",
+                   "prefill": {"B": pc.B, "H": pc.H, "N": pc.N, "d": pc.d, "causal": pc.causal},
+                   "decode": {"B": dc.B, "H": dc.H, "L": dc.L, "d": dc.d, "num_splits": splits},
+                   "l2": "inputs larger than L2 (prefill q/k/v/o 268 MB, decode KV 8.6 GB); no flush",
+                   "parallelism": f"replicas x{world}"},
+        "decode": {"value": dec_gbs, "unit": "GB/s (KV read)", "frac_of_hbm": dec_gbs / peaks["hbm_gbs"],
+                   "ms_per_step": dec_avg_ms},
+        "prefill_ms_per_step": fwd_avg_ms,
+        "prefill_frac_of_bf16_peak": value / world / tflops_peak,
+        "roofline": dominant,
+        "rooflines": {"fwd": fwd_roof, "decode": dec_roof},
+        "cpu_baseline": {"value": c_tflops, "unit": "TFLOP/s", "cores": _cores(), "kind": "oracle",
+                         "sample": c_desc, "seconds": c_dt},
+        "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "steps": e2e_steps, "what": "prefill through fa_fwd with pinned host buffers"},
+        "gpu_launches": 3 * args.steps,
+        "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--splits", type=int, default=DEFAULT_SPLITS)
+    ap.add_argument("--cpu-heads", type=int, default=4)
+    args = ap.parse_args()
+    world, rank, local = _dist()
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+        return
+    run_gpu(args, world, rank, local)
+
+
+if __name__ == "__main__":
+    main()

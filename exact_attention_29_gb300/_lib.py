@@ -1,0 +1,180 @@
+"""ctypes binding of libfa.so: argument marshalling only.
+
+Every function here checks tensor shapes/dtypes/devices, turns tensors into
+raw device pointers and the current torch stream into a cudaStream_t, calls
+the C ABI of the same name, and raises ``FaError`` on a non-OK status. All
+arithmetic runs in the CUDA kernels; there is no fallback of any kind. If
+``libfa.so`` is missing the first call raises ``RuntimeError``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libfa.so")
+
+FA_OK = 0
+FA_ERR_INVALID_ARG = 1
+FA_ERR_UNSUPPORTED = 2
+FA_ERR_CUDA = 3
+FA_ERR_TIMEOUT = 4
+
+_lib = None
+_lock = threading.Lock()
+
+_VP = ctypes.c_void_p
+_I = ctypes.c_int
+_SIGNATURES = {
+    "fa_fwd": ([_VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, ctypes.c_float, _VP], _I),
+    "fa_decode": ([_VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _VP], _I),
+    "fa_status_string": ([_I], ctypes.c_char_p),
+    "fa_last_error_string": ([], ctypes.c_char_p),
+    "fa_check_device_error": ([_VP, ctypes.POINTER(_I)], _I),
+    "fa_fwd_plan": ([_I, _I, _I, ctypes.POINTER(ctypes.c_longlong), ctypes.POINTER(ctypes.c_longlong)], _I),
+    "fa_selftest_mma": ([_I, _VP, _VP, _VP, _I, _I, _VP], _I),
+    "fa_selftest_wait_timeout": ([ctypes.c_uint, _VP], _I),
+}
+
+
+class FaError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        lib = _lib
+        text = lib.fa_status_string(status).decode() if lib else str(status)
+        detail = lib.fa_last_error_string().decode() if (lib and status == FA_ERR_CUDA) else ""
+        super().__init__(f"{where}: {text}" + (f" [{detail}]" if detail else ""))
+
+
+def load_library() -> ctypes.CDLL:
+    """Load libfa.so (once). Raises RuntimeError if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(f"{LIB_PATH} is missing: build it with `python -m exact_attention_29_gb300.build` "
+                                   "(the CUDA library is required; there is no fallback)")
+            lib = ctypes.CDLL(LIB_PATH)
+            for name, (argtypes, restype) in _SIGNATURES.items():
+                fn = getattr(lib, name)
+                fn.argtypes = argtypes
+                fn.restype = restype
+            _lib = lib
+    return _lib
+
+
+def _check(status: int, where: str) -> None:
+    if status != FA_OK:
+        raise FaError(status, where)
+
+
+def _stream_handle(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream)
+
+
+def _require(t: torch.Tensor, name: str, dtype, ndim: int) -> None:
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.device.type != "cuda":
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dimensions, got {t.dim()}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def fa_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = False, scale: float | None = None,
+           o: torch.Tensor | None = None, lse: torch.Tensor | None = None, stream=None):
+    """Fused prefill attention. q, k, v: bf16 [B, H, N, d] on the GPU.
+
+    Returns (o bf16 [B, H, N, d], lse fp32 [B, H, N]); enqueued on ``stream``
+    (default: the current torch stream).
+    """
+    lib = load_library()
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _require(t, n, torch.bfloat16, 4)
+    if k.shape != q.shape or v.shape != q.shape:
+        raise ValueError("q, k and v must have the same shape [B, H, N, d]")
+    B, H, N, d = q.shape
+    if scale is None:
+        scale = d ** -0.5
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    _require(o, "o", torch.bfloat16, 4)
+    _require(lse, "lse", torch.float32, 3)
+    if o.shape != q.shape or lse.shape != (B, H, N):
+        raise ValueError("o must match q and lse must be [B, H, N]")
+    st = lib.fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), B, H, N, d,
+                    1 if causal else 0, float(scale), _stream_handle(stream))
+    _check(st, "fa_fwd")
+    return o, lse
+
+
+def fa_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, seqlens: torch.Tensor,
+              num_splits: int, o: torch.Tensor | None = None, lse: torch.Tensor | None = None, stream=None):
+    """Flash-Decoding. q bf16 [B, H, d]; caches bf16 [B, H, L, d]; seqlens int32 [B] on the GPU.
+
+    Returns (o bf16 [B, H, d], lse fp32 [B, H]).
+    """
+    lib = load_library()
+    _require(q, "q", torch.bfloat16, 3)
+    _require(k_cache, "k_cache", torch.bfloat16, 4)
+    _require(v_cache, "v_cache", torch.bfloat16, 4)
+    _require(seqlens, "seqlens", torch.int32, 1)
+    B, H, L, d = k_cache.shape
+    if v_cache.shape != k_cache.shape or q.shape != (B, H, d) or seqlens.shape != (B,):
+        raise ValueError("shapes must be q [B,H,d], caches [B,H,L,d], seqlens [B]")
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H), dtype=torch.float32, device=q.device)
+    _require(o, "o", torch.bfloat16, 3)
+    _require(lse, "lse", torch.float32, 2)
+    st = lib.fa_decode(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), seqlens.data_ptr(), o.data_ptr(),
+                       lse.data_ptr(), B, H, L, d, int(num_splits), _stream_handle(stream))
+    _check(st, "fa_decode")
+    return o, lse
+
+
+def fa_check_device_error(stream=None) -> int:
+    """Synchronise the stream and return the site code of a kernel wait that ran out
+    (0 if none); raises FaError(FA_ERR_TIMEOUT) when one did."""
+    lib = load_library()
+    site = ctypes.c_int(0)
+    st = lib.fa_check_device_error(_stream_handle(stream), ctypes.byref(site))
+    if st == FA_ERR_TIMEOUT:
+        err = FaError(st, f"fa_check_device_error (site {site.value})")
+        err.site = site.value
+        raise err
+    _check(st, "fa_check_device_error")
+    return site.value
+
+
+def fa_fwd_plan(N: int, block: int = 128, causal: bool = False):
+    """(pairs_total, pairs_computed) of the prefill tile plan; host only."""
+    lib = load_library()
+    tot, done = ctypes.c_longlong(0), ctypes.c_longlong(0)
+    _check(lib.fa_fwd_plan(N, block, 1 if causal else 0, ctypes.byref(tot), ctypes.byref(done)), "fa_fwd_plan")
+    return tot.value, done.value
+
+
+def fa_selftest_mma(mode: int, a: torch.Tensor, b: torch.Tensor, n: int, k: int, stream=None) -> torch.Tensor:
+    lib = load_library()
+    d = torch.empty((128, n), dtype=torch.float32, device=a.device)
+    _check(lib.fa_selftest_mma(mode, a.data_ptr(), b.data_ptr(), d.data_ptr(), n, k, _stream_handle(stream)),
+           "fa_selftest_mma")
+    return d
+
+
+def fa_selftest_wait_timeout(timeout_us: int, stream=None) -> None:
+    lib = load_library()
+    _check(lib.fa_selftest_wait_timeout(int(timeout_us), _stream_handle(stream)), "fa_selftest_wait_timeout")

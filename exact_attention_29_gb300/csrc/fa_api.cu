@@ -1,0 +1,249 @@
+// C ABI of libfa.so (declared in include/fa.h): argument checks, per-device
+// lookups, tensor-map encoding, the device error word, and dispatch to the
+// kernels. No attention arithmetic lives here.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "fa_common.cuh"
+#include "fa_internal.h"
+
+namespace fa {
+
+// The device error word (flags, first site); see fa_common.cuh.
+__device__ unsigned int g_error_word[2];
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+thread_local char t_error_text[512] = "";
+
+std::mutex g_mutex;
+unsigned int* g_err_ptr[kMaxDevices] = {};
+int g_dev_ok[kMaxDevices] = {};  // 0 unknown, 1 sm_103, -1 other
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+// Current device, checked once to be compute capability 10.3.
+fa_status current_device(int* dev_out) {
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) {
+    set_error_text("cudaGetDevice", e);
+    return FA_ERR_CUDA;
+  }
+  if (dev < 0 || dev >= kMaxDevices) {
+    set_error_text("device index", "out of range");
+    return FA_ERR_UNSUPPORTED;
+  }
+  std::lock_guard<std::mutex> lock(g_mutex);
+  if (g_dev_ok[dev] == 0) {
+    int major = 0, minor = 0;
+    e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    if (e != cudaSuccess) {
+      set_error_text("cudaDeviceGetAttribute", e);
+      return FA_ERR_CUDA;
+    }
+    g_dev_ok[dev] = (major == 10 && minor == 3) ? 1 : -1;
+  }
+  if (g_dev_ok[dev] != 1) {
+    set_error_text("device", "kernels are built for sm_103a only");
+    return FA_ERR_UNSUPPORTED;
+  }
+  *dev_out = dev;
+  return FA_OK;
+}
+
+}  // namespace
+
+void set_error_text(const char* what, cudaError_t err) {
+  std::snprintf(t_error_text, sizeof(t_error_text), "%s: %s (%s)", what, cudaGetErrorName(err),
+                cudaGetErrorString(err));
+}
+
+void set_error_text(const char* what, const char* detail) {
+  std::snprintf(t_error_text, sizeof(t_error_text), "%s: %s", what, detail);
+}
+
+unsigned int* device_error_word() {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  if (g_err_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_error_word);
+    if (e != cudaSuccess) {
+      set_error_text("cudaGetSymbolAddress(g_error_word)", e);
+      return nullptr;
+    }
+    g_err_ptr[dev] = static_cast<unsigned int*>(p);
+  }
+  return g_err_ptr[dev];
+}
+
+bool encode_bf16_map(CUtensorMap* map, const void* base, uint64_t d, uint64_t rows, uint64_t outer,
+                     uint32_t box_rows) {
+  {
+    std::lock_guard<std::mutex> lock(g_mutex);
+    if (g_encode == nullptr) {
+      void* fn = nullptr;
+      cudaDriverEntryPointQueryResult q;
+      const cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                             cudaEnableDefault, &q);
+      if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || fn == nullptr) {
+        set_error_text("cudaGetDriverEntryPointByVersion(cuTensorMapEncodeTiled)", e);
+        return false;
+      }
+      g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+    }
+  }
+  const cuuint64_t dims[3] = {d, rows, outer};
+  const cuuint64_t strides[2] = {d * 2, rows * d * 2};
+  const cuuint32_t box[3] = {64, box_rows, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+                              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    char buf[64];
+    std::snprintf(buf, sizeof(buf), "CUresult %d", static_cast<int>(r));
+    set_error_text("cuTensorMapEncodeTiled", buf);
+    return false;
+  }
+  return true;
+}
+
+}  // namespace fa
+
+using namespace fa;
+
+extern "C" {
+
+const char* fa_status_string(fa_status status) {
+  switch (status) {
+    case FA_OK: return "FA_OK";
+    case FA_ERR_INVALID_ARG: return "FA_ERR_INVALID_ARG: invalid argument";
+    case FA_ERR_UNSUPPORTED: return "FA_ERR_UNSUPPORTED: unsupported head dimension or device";
+    case FA_ERR_CUDA: return "FA_ERR_CUDA: a CUDA call failed";
+    case FA_ERR_TIMEOUT: return "FA_ERR_TIMEOUT: a bounded wait inside a kernel ran out";
+  }
+  return "unknown fa_status";
+}
+
+const char* fa_last_error_string(void) { return t_error_text; }
+
+fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
+                 int causal, float scale, fa_stream_t stream) {
+  if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned4(lse)) return FA_ERR_INVALID_ARG;
+  if (B < 1 || H < 1 || N < 1 || d < 1) return FA_ERR_INVALID_ARG;
+  if (!(scale > 0.f) || !std::isfinite(scale)) return FA_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  const long long bh = static_cast<long long>(B) * H;
+  const long long pairs = (static_cast<long long>(N) + 255) / 256;
+  if (bh > 0x7fffffffLL || pairs > 65535) return FA_ERR_INVALID_ARG;
+  int dev = -1;
+  fa_status st = current_device(&dev);
+  if (st != FA_OK) return st;
+  unsigned int* err = device_error_word();
+  if (!err) return FA_ERR_CUDA;
+  return launch_fwd(q, k, v, o, lse, B, H, N, d, causal, scale, reinterpret_cast<cudaStream_t>(stream), err);
+}
+
+fa_status fa_decode(const void* q, const void* k_cache, const void* v_cache, const int32_t* seqlens, void* o,
+                    float* lse, int B, int H, int L, int d, int num_splits, fa_stream_t stream) {
+  if (!q || !k_cache || !v_cache || !seqlens || !o || !lse) return FA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned4(seqlens) || !aligned4(o) ||
+      !aligned4(lse))
+    return FA_ERR_INVALID_ARG;
+  if (B < 1 || H < 1 || L < 1 || d < 1) return FA_ERR_INVALID_ARG;
+  if (num_splits < 1 || num_splits > 64) return FA_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  if (static_cast<long long>(B) * H > 0x7fffffffLL || H > 65535 || B > 65535) return FA_ERR_INVALID_ARG;
+  int dev = -1;
+  fa_status st = current_device(&dev);
+  if (st != FA_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const size_t parts = static_cast<size_t>(B) * H * num_splits;
+  void* ws = nullptr;
+  cudaError_t e = cudaMallocAsync(&ws, parts * (d + 1) * sizeof(float), s);
+  if (e != cudaSuccess) {
+    set_error_text("cudaMallocAsync(decode workspace)", e);
+    return FA_ERR_CUDA;
+  }
+  float* ws_o = static_cast<float*>(ws);
+  float* ws_lse = ws_o + parts * d;
+  st = launch_decode(q, k_cache, v_cache, seqlens, o, lse, B, H, L, d, num_splits, ws_o, ws_lse, s);
+  e = cudaFreeAsync(ws, s);
+  if (st == FA_OK && e != cudaSuccess) {
+    set_error_text("cudaFreeAsync(decode workspace)", e);
+    st = FA_ERR_CUDA;
+  }
+  return st;
+}
+
+fa_status fa_check_device_error(fa_stream_t stream, int* site) {
+  if (site) *site = 0;
+  cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) {
+    set_error_text("cudaStreamSynchronize", e);
+    return FA_ERR_CUDA;
+  }
+  unsigned int* err = device_error_word();
+  if (!err) return FA_ERR_CUDA;
+  unsigned int host[2] = {0, 0};
+  e = cudaMemcpy(host, err, sizeof(host), cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess && host[0] != 0) e = cudaMemset(err, 0, sizeof(host));
+  if (e != cudaSuccess) {
+    set_error_text("reading the device error word", e);
+    return FA_ERR_CUDA;
+  }
+  if (site) *site = static_cast<int>(host[1]);
+  return (host[0] & kErrTimeout) ? FA_ERR_TIMEOUT : FA_OK;
+}
+
+fa_status fa_fwd_plan(int N, int block, int causal, long long* pairs_total, long long* pairs_computed) {
+  if (N < 1 || block < 1 || !pairs_total || !pairs_computed) return FA_ERR_INVALID_ARG;
+  const long long t = (static_cast<long long>(N) + block - 1) / block;
+  long long done = 0;
+  for (long long i = 0; i < t; ++i) done += fwd_kv_tiles(static_cast<int>(i * block), N, block, causal);
+  *pairs_total = t * t;
+  *pairs_computed = done;
+  return FA_OK;
+}
+
+fa_status fa_selftest_mma(int mode, const void* a, const void* b, float* d, int n, int k, fa_stream_t stream) {
+  if (!a || !b || !d || !aligned16(a) || !aligned16(b) || !aligned4(d)) return FA_ERR_INVALID_ARG;
+  if (mode != 0 && mode != 1) return FA_ERR_INVALID_ARG;
+  int dev = -1;
+  fa_status st = current_device(&dev);
+  if (st != FA_OK) return st;
+  unsigned int* err = device_error_word();
+  if (!err) return FA_ERR_CUDA;
+  return launch_selftest_mma(mode, a, b, d, n, k, reinterpret_cast<cudaStream_t>(stream), err);
+}
+
+fa_status fa_selftest_wait_timeout(unsigned int timeout_us, fa_stream_t stream) {
+  if (timeout_us == 0 || timeout_us > 5000000u) return FA_ERR_INVALID_ARG;
+  int dev = -1;
+  fa_status st = current_device(&dev);
+  if (st != FA_OK) return st;
+  unsigned int* err = device_error_word();
+  if (!err) return FA_ERR_CUDA;
+  return launch_selftest_wait(timeout_us, reinterpret_cast<cudaStream_t>(stream), err);
+}
+
+}  // extern "C"

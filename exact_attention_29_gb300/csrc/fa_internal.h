@@ -1,0 +1,36 @@
+// Host-side interfaces between the translation units of libfa.so.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "../../include/fa.h"
+
+namespace fa {
+
+// Encode a 3-D bf16 tensor map over [outer][rows][d] with a {64, box_rows, 1}
+// box and 128-byte swizzle. Returns false (and sets the error text) on failure.
+bool encode_bf16_map(CUtensorMap* map, const void* base, uint64_t d, uint64_t rows, uint64_t outer,
+                     uint32_t box_rows);
+
+// Record the text of a CUDA failure for fa_last_error_string.
+void set_error_text(const char* what, cudaError_t err);
+void set_error_text(const char* what, const char* detail);
+
+// Device error word of the current device (see fa_common.cuh).
+unsigned int* device_error_word();
+
+fa_status launch_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
+                     int causal, float scale, cudaStream_t stream, unsigned int* err);
+
+fa_status launch_decode(const void* q, const void* k_cache, const void* v_cache, const int32_t* seqlens, void* o,
+                        float* lse, int B, int H, int L, int d, int num_splits, float* ws_o, float* ws_lse,
+                        cudaStream_t stream);
+
+fa_status launch_selftest_mma(int mode, const void* a, const void* b, float* d, int n, int k, cudaStream_t stream,
+                              unsigned int* err);
+fa_status launch_selftest_wait(unsigned int timeout_us, cudaStream_t stream, unsigned int* err);
+
+}  // namespace fa

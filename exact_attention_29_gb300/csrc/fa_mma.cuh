@@ -1,0 +1,45 @@
+// Tile geometry and the two tensor-core products of the attention forward,
+// shared by the prefill kernel and the tensor-core self-test.
+//
+// Shared-memory tiles are 128 rows of bf16, written by TMA with 128-byte
+// swizzle: each 64-element (128-byte) slice of d forms a 16 KB "chunk" of
+// 128 rows x 128 bytes, and chunks are stored one after the other.
+#pragma once
+
+#include <cstdint>
+
+#include "sm103.cuh"
+
+namespace fa {
+
+constexpr int kBM = 128;               // query rows per Q tile (= TMEM lanes)
+constexpr int kBN = 128;               // keys per K/V tile
+constexpr int kChunkBytes = 128 * 128; // one 128-row x 128-byte swizzle chunk
+
+// S(tmem, 128 x 128 fp32) = Q(smem, 128 x D, K-major) * K(smem, 128 x D, K-major)^T
+template <int D>
+__device__ __forceinline__ void issue_qk(uint32_t s_tmem, uint32_t q_smem, uint32_t k_smem) {
+  constexpr uint32_t idesc = idesc_bf16_f32(kBM, kBN, false, false);
+#pragma unroll
+  for (int kk = 0; kk < D / 16; ++kk) {
+    // 16 bf16 = 32 bytes of the 128-byte swizzled row; 4 steps per chunk
+    const uint32_t off = static_cast<uint32_t>((kk / 4) * kChunkBytes + (kk % 4) * 32);
+    umma_ss(s_tmem, smem_desc_sw128(q_smem + off, 16, 1024), smem_desc_sw128(k_smem + off, 16, 1024), idesc,
+            kk > 0 ? 1u : 0u);
+  }
+}
+
+// O(tmem, 128 x D fp32) (+)= P(tmem, 128 x 128 bf16, packed pairs) * V(smem, 128 keys x D, MN-major)
+template <int D>
+__device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem, uint32_t v_smem, bool accumulate) {
+  constexpr uint32_t idesc = idesc_bf16_f32(kBM, D, false, true);
+#pragma unroll
+  for (int kk = 0; kk < kBN / 16; ++kk) {
+    // 16 keys = two 8-row groups of 1024 bytes; P advances 8 packed columns
+    umma_ts(o_tmem, p_tmem + static_cast<uint32_t>(kk * 8),
+            smem_desc_sw128(v_smem + static_cast<uint32_t>(kk * 2048), kChunkBytes, 1024), idesc,
+            (accumulate || kk > 0) ? 1u : 0u);
+  }
+}
+
+}  // namespace fa

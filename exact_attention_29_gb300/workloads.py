@@ -27,7 +27,7 @@ from dataclasses import dataclass
 
 import torch
 
-GPU_GEN_THRESHOLD = 1 << 28  # elements per tensor
+GPU_GEN_THRESHOLD = 1 << 25  # elements per tensor
 
 
 @dataclass(frozen=True)

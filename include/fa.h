@@ -1,0 +1,145 @@
+/*
+ * fa.h — C ABI of the GB300 exact-attention library (libfa.so).
+ *
+ * Two operations, both exact (no approximation beyond floating-point rounding):
+ *
+ *   fa_fwd     fused prefill attention O = softmax(scale * Q K^T [+ causal mask]) V
+ *              with the per-row log-sum-exp written out; the N x N score and
+ *              probability matrices never reach device memory.
+ *   fa_decode  Flash-Decoding: one query token per (batch, head) against a long
+ *              KV cache, split along the keys, the per-split summaries merged
+ *              by the log-sum-exp combine.
+ *
+ * Conventions for every call:
+ *   - Tensor arguments are DEVICE pointers (memory of the current CUDA device),
+ *     owned by the caller, contiguous, row-major in the layout stated. The
+ *     library keeps no reference to them after the call returns.
+ *   - bf16 means IEEE bfloat16 (torch.bfloat16); outputs are rounded to nearest
+ *     even. Arithmetic is fp32 (tensor-core accumulation, softmax statistics).
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream). Calls only
+ *     enqueue work on it and return; results are ready when the stream is.
+ *   - Argument errors are reported before anything is enqueued. Launch errors
+ *     are returned at once. Errors found while the kernels run (a bounded wait
+ *     inside a kernel that ran out) are reported by fa_check_device_error.
+ *   - The library is thread-safe; it holds no state besides per-device lookups.
+ */
+#ifndef FA_H_
+#define FA_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t (declared here so the header needs no CUDA headers). */
+typedef struct CUstream_st *fa_stream_t;
+
+typedef enum {
+  FA_OK = 0,
+  FA_ERR_INVALID_ARG = 1,  /* null pointer, non-positive size, misaligned pointer, bad scale */
+  FA_ERR_UNSUPPORTED = 2,  /* valid but not implemented here (head dim other than 64 or 128, no sm_103 device) */
+  FA_ERR_CUDA = 3,         /* a CUDA runtime or driver call failed; see fa_last_error_string() */
+  FA_ERR_TIMEOUT = 4       /* a kernel's bounded wait ran out; the kernel stopped and its outputs are undefined */
+} fa_status;
+
+/*
+ * Prefill (forward) attention.
+ *
+ * Defines: "已有的几种大模型上下文支持情况" (cicada blog) §1.2
+ *   Attention(Q,K,V) = softmax(Q K^T / sqrt(d_k)) V, §1.3 (causal mask sets
+ *   future positions to -inf) and §3.2 (FlashAttention-2: tiles of Q stay on
+ *   chip, K/V tiles stream through, running max m and normaliser l, one divide
+ *   by l at the end, L_i = m_i + ln l_i written out); CMU 15-779 Lecture 5
+ *   notes §5.1 (the tiled forward) and §6.2 (causal block skipping).
+ *
+ *   q, k, v  bf16 [B][H][N][d], d contiguous. 16-byte aligned.
+ *   o        bf16 [B][H][N][d] output.
+ *   lse      fp32 [B][H][N] output: natural log of sum_j exp(scale * q_i . k_j)
+ *            over the keys row i sees.
+ *   B, H, N  >= 1 (N need not be a multiple of any tile size).
+ *   d        64 or 128 (FA_ERR_UNSUPPORTED otherwise).
+ *   causal   0: every row sees all N keys; 1: row i sees keys 0..i.
+ *   scale    > 0 and finite, usually 1/sqrt(d).
+ * Errors: FA_ERR_INVALID_ARG for null/misaligned pointers, sizes < 1, a bad
+ *   scale, or sizes whose element counts overflow; FA_ERR_UNSUPPORTED for d;
+ *   FA_ERR_CUDA if the launch fails.
+ */
+fa_status fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H, int N, int d,
+                 int causal, float scale, fa_stream_t stream);
+
+/*
+ * Decode attention (Flash-Decoding).
+ *
+ * Defines: CMU 15-779 Lecture 5 notes §8.4 (split K/V along the sequence into
+ *   S views; one thread block per split computes a partial result and its
+ *   log-sum-exp; a small reduction kernel reweights the partials by their
+ *   log-sum-exp), §4.4-4.5 (the combine operator on (m, l, o)) and §8.2 (the
+ *   cached step equals the last row of the causal recomputation).
+ *
+ *   q        bf16 [B][H][d], the single new query of each (batch, head).
+ *   k_cache, v_cache  bf16 [B][H][L][d]; L is the cache capacity.
+ *   seqlens  DEVICE int32 [B]; sequence b uses cache entries 0..seqlens[b]-1.
+ *            Values must lie in 1..L (entries outside are clamped in-kernel to
+ *            0..L; a length of 0 gives lse = -inf and o = 0).
+ *   o        bf16 [B][H][d] output; lse fp32 [B][H] output (natural log).
+ *   d        64 or 128. scale is fixed at 1/sqrt(d).
+ *   num_splits  1..64: keys of each sequence are cut into num_splits chunks of
+ *            ceil(len/num_splits) rounded up to a multiple of 64 keys.
+ * Workspace: the call allocates B*H*num_splits*(d+1)*4 bytes of stream-ordered
+ *   device memory (cudaMallocAsync) and frees it on the same stream.
+ * Errors: as fa_fwd; FA_ERR_INVALID_ARG also for num_splits outside 1..64.
+ */
+fa_status fa_decode(const void *q, const void *k_cache, const void *v_cache, const int32_t *seqlens, void *o,
+                    float *lse, int B, int H, int L, int d, int num_splits, fa_stream_t stream);
+
+/* Static text for a status code. Never NULL. */
+const char *fa_status_string(fa_status status);
+
+/* Text of the most recent FA_ERR_CUDA on the calling thread ("" if none). */
+const char *fa_last_error_string(void);
+
+/*
+ * Synchronise `stream`, then read and clear the device error word of the
+ * current device. Returns FA_ERR_TIMEOUT if a kernel recorded that one of its
+ * bounded waits ran out since the last check, FA_ERR_CUDA if the stream
+ * reports an error, FA_OK otherwise. `site`, if not NULL, receives the code of
+ * the first wait that ran out (0 if none).
+ */
+fa_status fa_check_device_error(fa_stream_t stream, int *site);
+
+/*
+ * Work plan of fa_fwd (host only, no device needed): with square tiles of
+ * `block` rows, count the (Q tile, K/V tile) pairs of an N x N problem and how
+ * many of them the kernel computes. Causal mode skips every pair that lies
+ * entirely above the diagonal (CMU 15-779 Lecture 5 notes §6.2: T(T+1)/2 of
+ * T^2 pairs). fa_fwd uses block = 128.
+ */
+fa_status fa_fwd_plan(int N, int block, int causal, long long *pairs_total, long long *pairs_computed);
+
+/*
+ * Self-tests of the kernels' building blocks (used by the test suite).
+ *
+ * fa_selftest_mma: one 128 x n x k product on the tensor cores through the same
+ *   staging the attention kernel uses (TMA with 128-byte swizzle into shared
+ *   memory, tcgen05.mma with an fp32 accumulator in tensor memory).
+ *   mode 0: D[128][n] = A[128][k] * B[n][k]^T, A and B K-major in shared memory
+ *           (the S = Q K^T product), n = 128, k in {64, 128}.
+ *   mode 1: D[128][n] = A[128][k] * B[k][n], A placed in tensor memory as packed
+ *           bf16 pairs, B MN-major in shared memory (the O += P V product),
+ *           k = 128, n in {64, 128}.
+ *   a, b: bf16 device pointers; d: fp32 device pointer [128][n].
+ *
+ * fa_selftest_wait_timeout: launch one block that waits on a barrier nothing
+ *   ever arrives at, bounded by `timeout_us`; the kernel gives up, records
+ *   the timeout in the device error word and returns. fa_check_device_error
+ *   then reports FA_ERR_TIMEOUT.
+ */
+fa_status fa_selftest_mma(int mode, const void *a, const void *b, float *d, int n, int k, fa_stream_t stream);
+fa_status fa_selftest_wait_timeout(unsigned int timeout_us, fa_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_H_ */

@@ -118,14 +118,18 @@ int oracle_attention_rows(const double *q, const int *q_pos, const double *k,
     l[i] = li;
   }
 
-  /* Step 4: O = P V and LSE = m + ln(l). */
+  /* Step 4: O = P V and LSE = m + ln(l). Each O[i][c] is the sum over keys
+   * j = 0, 1, ... of P[i][j] * V[j][c], accumulated in ascending j; the j loop
+   * is outside the c loop only so that V is read row by row. */
 #pragma omp parallel for schedule(static)
   for (int i = 0; i < n_rows; ++i) {
     const double *Pi = P + (size_t)i * n_keys;
-    for (int c = 0; c < d; ++c) {
-      double acc = 0.0;
-      for (int j = 0; j < n_keys; ++j) acc += Pi[j] * v[(size_t)j * d + c];
-      o[(size_t)i * d + c] = acc;
+    double *Oi = o + (size_t)i * d;
+    for (int c = 0; c < d; ++c) Oi[c] = 0.0;
+    for (int j = 0; j < n_keys; ++j) {
+      const double pij = Pi[j];
+      const double *Vj = v + (size_t)j * d;
+      for (int c = 0; c < d; ++c) Oi[c] += pij * Vj[c];
     }
     lse[i] = m[i] + log(l[i]);
   }

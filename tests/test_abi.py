@@ -1,0 +1,156 @@
+"""The C ABI library on the CPU: it builds, loads, exports every declared symbol,
+and rejects bad arguments before touching the GPU. No compute calls here."""
+import ctypes
+import json
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fa.h")
+GOLDEN = os.path.join(ROOT, "tests", "golden")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from exact_attention_29_gb300 import build
+
+    build.build()
+    import exact_attention_29_gb300 as fa
+
+    return fa.load_library()
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return re.findall(r"^\s*(?:fa_status|const\s+char\s*\*)\s*\*?\s*(fa_\w+)\s*\(", text, flags=re.M)
+
+
+def test_header_declares_the_boundary():
+    names = _declared_functions()
+    for required in ("fa_fwd", "fa_decode", "fa_status_string", "fa_check_device_error"):
+        assert required in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = _declared_functions()
+    assert names
+    for name in names:
+        assert hasattr(lib, name), f"libfa.so does not export {name}"
+
+
+def test_status_strings(lib):
+    for code in range(5):
+        s = lib.fa_status_string(code)
+        assert s and s.startswith(b"FA_")
+    assert lib.fa_status_string(99) == b"unknown fa_status"
+
+
+def _fwd(lib, q=16, k=16, v=16, o=16, lse=16, B=1, H=1, N=128, d=64, causal=0, scale=0.125):
+    return lib.fa_fwd(q, k, v, o, lse, B, H, N, d, causal, scale, None)
+
+
+def test_fwd_rejects_bad_arguments(lib):
+    import exact_attention_29_gb300 as fa
+
+    assert _fwd(lib, q=None) == fa.FA_ERR_INVALID_ARG
+    assert _fwd(lib, lse=None) == fa.FA_ERR_INVALID_ARG
+    assert _fwd(lib, k=24) == fa.FA_ERR_INVALID_ARG  # not 16-byte aligned
+    assert _fwd(lib, N=0) == fa.FA_ERR_INVALID_ARG
+    assert _fwd(lib, B=-1) == fa.FA_ERR_INVALID_ARG
+    assert _fwd(lib, scale=0.0) == fa.FA_ERR_INVALID_ARG
+    assert _fwd(lib, scale=float("inf")) == fa.FA_ERR_INVALID_ARG
+    assert _fwd(lib, scale=float("nan")) == fa.FA_ERR_INVALID_ARG
+    assert _fwd(lib, causal=2) == fa.FA_ERR_INVALID_ARG
+    assert _fwd(lib, d=96) == fa.FA_ERR_UNSUPPORTED
+    assert _fwd(lib, d=256) == fa.FA_ERR_UNSUPPORTED
+    assert _fwd(lib, N=65536 * 256 + 1) == fa.FA_ERR_INVALID_ARG  # more Q-tile pairs than the grid allows
+
+
+def test_decode_rejects_bad_arguments(lib):
+    import exact_attention_29_gb300 as fa
+
+    def dec(num_splits=8, d=128, L=64, seqlens=16, q=16):
+        return lib.fa_decode(q, 16, 16, seqlens, 16, 16, 1, 1, L, d, num_splits, None)
+
+    assert dec(num_splits=0) == fa.FA_ERR_INVALID_ARG
+    assert dec(num_splits=65) == fa.FA_ERR_INVALID_ARG
+    assert dec(seqlens=None) == fa.FA_ERR_INVALID_ARG
+    assert dec(q=8) == fa.FA_ERR_INVALID_ARG
+    assert dec(L=0) == fa.FA_ERR_INVALID_ARG
+    assert dec(d=80) == fa.FA_ERR_UNSUPPORTED
+
+
+def test_selftests_reject_bad_arguments(lib):
+    import exact_attention_29_gb300 as fa
+
+    assert lib.fa_selftest_wait_timeout(0, None) == fa.FA_ERR_INVALID_ARG
+    assert lib.fa_selftest_wait_timeout(10_000_000, None) == fa.FA_ERR_INVALID_ARG
+    assert lib.fa_selftest_mma(2, 16, 16, 16, 128, 128, None) == fa.FA_ERR_INVALID_ARG
+
+
+def test_causal_block_plan_matches_the_page(lib):
+    """CMU 15-779 Lecture 5 notes §6.2 and Exercise 5: T(T+1)/2 of T^2 block pairs
+    are computed; T = 4 gives 10/16 and K/V bytes 524,288 -> 327,680; T = 8 gives
+    36/64; T = 32 gives 51.6 %."""
+    import exact_attention_29_gb300 as fa
+
+    g = json.load(open(os.path.join(GOLDEN, "causal_block_counts.json")))
+    for case in g["cases"]:
+        tot, done = fa.fa_fwd_plan(case["N"], case["block"], causal=True)
+        assert tot == case["T"] ** 2
+        if "pairs_computed" in case:
+            assert done == case["pairs_computed"] and tot == case["pairs_total"]
+        if "kv_bytes_all" in case:
+            per_pair = 2 * case["block"] * case["d"] * case["elem_bytes"]
+            assert tot * per_pair == case["kv_bytes_all"] and done * per_pair == case["kv_bytes_computed"]
+        if "fraction_percent" in case:
+            assert round(100 * done / tot, 1) == case["fraction_percent"]
+        tot_nc, done_nc = fa.fa_fwd_plan(case["N"], case["block"], causal=False)
+        assert tot_nc == done_nc == tot
+
+
+def test_plan_ragged_and_tiny(lib):
+    import exact_attention_29_gb300 as fa
+
+    assert fa.fa_fwd_plan(1, 128, True) == (1, 1)
+    assert fa.fa_fwd_plan(129, 128, True) == (4, 3)
+    assert fa.fa_fwd_plan(129, 128, False) == (4, 4)
+    with pytest.raises(fa.FaError):
+        fa.fa_fwd_plan(0, 128, False)
+
+
+def test_io_model_matches_the_page():
+    """Lecture 5 notes Exercise 4: 2Nd + 2Nd N/B_r + N = 34.6 M elements for
+    N = 4096, d = 128, B_r = 128, of which about 97 % are K/V re-reads."""
+    from exact_attention_29_gb300 import perfmodel
+
+    g = json.load(open(os.path.join(GOLDEN, "io_counts.json")))
+    total = perfmodel.fwd_hbm_elements_tiled(g["N"], g["d"], g["B_r"])
+    assert total == sum(g["terms"].values())
+    assert round(total / 1e6, 1) == g["total_millions_printed"]
+    assert round(100 * g["terms"]["kv_rereads"] / total) == g["kv_share_percent_printed"]
+
+
+def test_flop_model():
+    from exact_attention_29_gb300 import perfmodel
+
+    # Llama-3-8B-shaped prefill: 2 * 32 * 4096^2 * 128 * 2 (causal half of 4 N^2 d per head)
+    assert perfmodel.fwd_flops(2, 32, 4096, 128, True) == 2 * 32 * 4096 ** 2 * 128 * 2
+    assert perfmodel.fwd_flops(1, 1, 10, 8, False) == 4 * 100 * 8
+    assert perfmodel.decode_kv_bytes(32, 128, [32768] * 16) == 16 * 32 * 32768 * 128 * 2 * 2
+
+
+def test_package_import_does_not_need_the_library(monkeypatch):
+    """Importing the binding is cheap; a missing library fails loudly on first use."""
+    import importlib
+
+    import exact_attention_29_gb300._lib as L
+
+    monkeypatch.setattr(L, "LIB_PATH", "/nonexistent/libfa.so")
+    monkeypatch.setattr(L, "_lib", None)
+    with pytest.raises(RuntimeError, match="missing"):
+        L.load_library()
+    importlib.reload(L)

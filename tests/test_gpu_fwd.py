@@ -1,0 +1,170 @@
+"""Prefill attention on the GPU (through the C ABI) against the fp64 oracle."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from exact_attention_29_gb300 import workloads as wl
+from parity import compare, require_gpu
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    require_gpu()
+    oracle.build()
+
+
+def _run(q, k, v, causal, scale=None):
+    import exact_attention_29_gb300 as fa
+
+    o, lse = fa.fa_fwd(q.cuda(), k.cuda(), v.cuda(), causal=causal, scale=scale)
+    fa.fa_check_device_error()
+    return o, lse
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("N", [1, 7, 128, 129, 200, 255, 256, 257, 384, 1000])
+def test_small_shapes_full_oracle(N, d, causal):
+    """Tiles are 128 rows, CTAs take 256 query rows: these sizes cover a single
+    row, partial tiles, an inactive second Q tile, ragged key tails and several
+    K/V tiles."""
+    B, H = (2, 2) if N <= 256 else (1, 2)
+    q, k, v = wl.prefill_inputs(B, H, N, d, seed=N + d)
+    o, lse = _run(q, k, v, causal)
+    o_ref, lse_ref = oracle.attention(q, k, v, causal, d ** -0.5)
+    compare(o, lse, o_ref, lse_ref, f"N={N} d={d} causal={causal}")
+
+
+def test_pr1_config():
+    """B=1, H=1, N=128, d=64, non-causal, seed 0 — the smallest named workload."""
+    c = wl.PREFILL["pr1"]
+    q, k, v = wl.prefill_inputs(c.B, c.H, c.N, c.d, seed=0)
+    o, lse = _run(q, k, v, c.causal)
+    o_ref, lse_ref = oracle.attention(q, k, v, c.causal, c.scale)
+    compare(o, lse, o_ref, lse_ref, "pr1")
+
+
+@pytest.mark.parametrize("name", ["gpt2_small", "gpt2_small_causal"])
+def test_gpt2_small_full_oracle(name):
+    c = wl.PREFILL[name]
+    q, k, v = wl.prefill_inputs(c.B, c.H, c.N, c.d, seed=0)
+    o, lse = _run(q, k, v, c.causal)
+    o_ref, lse_ref = oracle.attention(q, k, v, c.causal, c.scale)
+    compare(o, lse, o_ref, lse_ref, name)
+
+
+def _sampled_check(c, rows_per_head, heads=None, seed=0):
+    """Full-size run on the GPU; the oracle evaluates a seeded subset of rows of
+    each checked head (each a full row over its visible keys)."""
+    q, k, v = wl.prefill_inputs(c.B, c.H, c.N, c.d, seed=seed, device="cuda")
+    o, lse = _run(q, k, v, c.causal)
+    rows = wl.row_subsets(c.B, c.H, c.N, rows_per_head, seed=seed)
+    heads = heads or [(b, h) for b in range(c.B) for h in range(c.H)]
+    o_all, l_all, or_all, lr_all = [], [], [], []
+    for b, h in heads:
+        r = rows[b, h]
+        # always include the last row (the longest causal row) and row 0
+        r = torch.unique(torch.cat([r, torch.tensor([0, c.N - 1])]))
+        kk, vv = k[b, h].cpu(), v[b, h].cpu()
+        o_ref, lse_ref, _, _ = oracle.attention_rows(q[b, h, r.cuda()].cpu(), r.numpy(), kk, vv, c.causal, c.scale)
+        o_all.append(o[b, h, r.cuda()].cpu())
+        l_all.append(lse[b, h, r.cuda()].cpu())
+        or_all.append(o_ref)
+        lr_all.append(lse_ref)
+    compare(torch.cat(o_all), torch.cat(l_all), np.concatenate(or_all), np.concatenate(lr_all), c.name)
+    return o, lse
+
+
+def test_llama3_8b_prefill_sampled():
+    _sampled_check(wl.PREFILL["llama3_8b_prefill"], rows_per_head=64)
+
+
+def test_llama3_8b_prefill_noncausal_sampled():
+    _sampled_check(wl.PREFILL["llama3_8b_prefill_noncausal"], rows_per_head=32)
+
+
+def test_long_16k_sampled():
+    _sampled_check(wl.PREFILL["long_16k"], rows_per_head=256)
+
+
+def test_long_64k_sampled():
+    _sampled_check(wl.PREFILL["long_64k"], rows_per_head=256)
+
+
+def test_deterministic():
+    """No atomics in the forward: two runs are bitwise identical."""
+    q, k, v = wl.prefill_inputs(2, 4, 777, 128, seed=5)
+    o1, l1 = _run(q, k, v, True)
+    o2, l2 = _run(q, k, v, True)
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_causal_row0_is_v0():
+    """Row 0 sees only key 0: O_0 = V_0 (exactly, after bf16 rounding) and LSE_0 = scale q0.k0."""
+    q, k, v = wl.prefill_inputs(1, 3, 300, 64, seed=6)
+    o, lse = _run(q, k, v, True)
+    assert torch.equal(o[0, :, 0].cpu(), v[0, :, 0])
+    ref = (q[0, :, 0].double() * k[0, :, 0].double()).sum(-1) / 8.0
+    assert (lse[0, :, 0].double().cpu() - ref).abs().max().item() <= 1e-4
+
+
+def test_large_scores_rescale_path():
+    """Scores far beyond exp range (scale 1, inputs x4): the running max and the
+    conditional rescale of O must keep everything finite and exact."""
+    q, k, v = wl.prefill_inputs(1, 2, 640, 128, seed=7)
+    q = (q.float() * 4).to(torch.bfloat16)
+    # growing keys so the row max keeps rising tile after tile
+    ramp = torch.linspace(0.5, 3.0, 640).view(1, 1, 640, 1)
+    k = (k.float() * ramp).to(torch.bfloat16)
+    for causal in (False, True):
+        o, lse = _run(q, k, v, causal, scale=1.0)
+        o_ref, lse_ref = oracle.attention(q, k, v, causal, 1.0)
+        compare(o, lse, o_ref, lse_ref, f"large scores causal={causal}")
+
+
+def test_one_hot_dominant_rows():
+    """A key equal to 8x its query dominates the row: O row = that V row."""
+    q, k, v = wl.prefill_inputs(1, 1, 256, 64, seed=8)
+    for i, j in ((3, 200), (130, 10), (255, 255)):
+        k[0, 0, j] = (q[0, 0, i].float() * 8).to(torch.bfloat16)
+    o, lse = _run(q, k, v, False)
+    o_ref, lse_ref = oracle.attention(q, k, v, False, 0.125)
+    compare(o, lse, o_ref, lse_ref, "one-hot")
+    for i, j in ((3, 200), (130, 10), (255, 255)):
+        assert (o[0, 0, i].float().cpu() - v[0, 0, j].float()).abs().max().item() <= 2e-2
+
+
+def test_output_buffers_and_stream():
+    """Caller-provided outputs on a side stream are filled in place."""
+    import exact_attention_29_gb300 as fa
+
+    q, k, v = wl.prefill_inputs(1, 2, 300, 64, seed=9)
+    q, k, v = q.cuda(), k.cuda(), v.cuda()
+    o = torch.full_like(q, float("nan"))
+    lse = torch.full((1, 2, 300), float("nan"), device="cuda")
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        fa.fa_fwd(q, k, v, causal=True, o=o, lse=lse, stream=s)
+    s.synchronize()
+    fa.fa_check_device_error(s)
+    o_ref, lse_ref = oracle.attention(q.cpu(), k.cpu(), v.cpu(), True, 0.125)
+    compare(o, lse, o_ref, lse_ref, "side stream")
+
+
+def test_python_binding_rejects_bad_tensors():
+    import exact_attention_29_gb300 as fa
+
+    q = torch.zeros((1, 1, 8, 64), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(ValueError):
+        fa.fa_fwd(q.float(), q, q)
+    with pytest.raises(ValueError):
+        fa.fa_fwd(q.cpu(), q, q)
+    with pytest.raises(ValueError):
+        fa.fa_fwd(q, q[:, :, :4], q)
+    qq = torch.zeros((1, 1, 8, 96), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(fa.FaError) as e:
+        fa.fa_fwd(qq, qq, qq)
+    assert e.value.status == fa.FA_ERR_UNSUPPORTED

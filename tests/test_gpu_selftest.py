@@ -1,0 +1,59 @@
+"""GPU self-tests of the kernels' building blocks through the C ABI."""
+import numpy as np
+import pytest
+import torch
+
+from parity import require_gpu
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    require_gpu()
+
+
+def _rand(shape, seed):
+    g = torch.Generator().manual_seed(seed)
+    return torch.randn(shape, generator=g).to(torch.bfloat16)
+
+
+@pytest.mark.parametrize("k", [64, 128])
+def test_mma_qk_k_major(k):
+    """D = A B^T with both operands K-major in swizzled shared memory (the S = Q K^T product)."""
+    import exact_attention_29_gb300 as fa
+
+    a, b = _rand((128, k), 1), _rand((128, k), 2)
+    d = fa.fa_selftest_mma(0, a.cuda(), b.cuda(), 128, k)
+    fa.fa_check_device_error()
+    ref = a.double() @ b.double().T
+    err = (d.double().cpu() - ref).abs().max().item()
+    assert err <= 1e-3, err
+
+
+@pytest.mark.parametrize("n", [64, 128])
+def test_mma_pv_tmem_a_mn_major_b(n):
+    """D = A B with A (bf16 pairs) in tensor memory and B MN-major in shared memory (O += P V)."""
+    import exact_attention_29_gb300 as fa
+
+    a, b = _rand((128, 128), 3), _rand((128, n), 4)
+    d = fa.fa_selftest_mma(1, a.cuda(), b.cuda(), n, 128)
+    fa.fa_check_device_error()
+    ref = a.double() @ b.double()
+    err = (d.double().cpu() - ref).abs().max().item()
+    assert err <= 1e-3, err
+
+
+def test_bounded_wait_times_out_and_context_survives():
+    """A wait on a barrier nothing arrives at gives up after its limit, the host
+    reads FA_ERR_TIMEOUT, the word is cleared, and the GPU keeps working."""
+    import exact_attention_29_gb300 as fa
+
+    fa.fa_check_device_error()  # start clean
+    fa.fa_selftest_wait_timeout(20_000)
+    with pytest.raises(fa.FaError) as exc:
+        fa.fa_check_device_error()
+    assert exc.value.status == fa.FA_ERR_TIMEOUT and exc.value.site == 100
+    assert fa.fa_check_device_error() == 0
+    x = torch.ones(1024, device="cuda")
+    assert float(x.sum().item()) == 1024.0
