@@ -383,7 +383,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--splits", type=int, default=DEFAULT_SPLITS)
-    ap.add_argument("--cpu-heads", type=int, default=4)
+    ap.add_argument("--cpu-heads", type=int, default=48)
     args = ap.parse_args()
     world, rank, local = _dist()
     if args.impl == "reference":

@@ -1,0 +1,71 @@
+"""Run one named workload a few times on cuda:0 (for profilers such as ncu).
+
+    python -m exact_attention_29_gb300.run_case --workload llama3_8b_prefill --iters 3
+    python -m exact_attention_29_gb300.run_case --workload decode_32k --batch 4 --splits 16 --iters 3
+
+``--batch`` overrides B (to keep a profiled case small); inputs are drawn by
+the seeded generators of ``workloads.py``. Prints the device time per
+iteration measured with CUDA events.
+"""
+from __future__ import annotations
+
+import argparse
+import os
+import sys
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+
+def main():
+    import torch
+
+    import exact_attention_29_gb300 as fa
+    from exact_attention_29_gb300 import build
+    from exact_attention_29_gb300 import workloads as wl
+
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--workload", required=True, choices=sorted(list(wl.PREFILL) + list(wl.DECODE)))
+    ap.add_argument("--iters", type=int, default=3)
+    ap.add_argument("--batch", type=int, default=0)
+    ap.add_argument("--splits", type=int, default=16)
+    args = ap.parse_args()
+    build.build()
+    dev = torch.device("cuda:0")
+    stream = torch.cuda.current_stream(dev)
+    if args.workload in wl.PREFILL:
+        c = wl.PREFILL[args.workload]
+        B = args.batch or c.B
+        q, k, v = wl.prefill_inputs(B, c.H, c.N, c.d, seed=0, device=dev)
+        o = torch.empty_like(q)
+        lse = torch.empty((B, c.H, c.N), dtype=torch.float32, device=dev)
+
+        def run():
+            fa.fa_fwd(q, k, v, causal=c.causal, o=o, lse=lse, stream=stream)
+    else:
+        c = wl.DECODE[args.workload]
+        B = args.batch or c.B
+        q, kc, vc, sl = wl.decode_inputs(B, c.H, c.L, c.d, seed=0, ragged=c.ragged, device=dev)
+        o = torch.empty_like(q)
+        lse = torch.empty((B, c.H), dtype=torch.float32, device=dev)
+
+        def run():
+            fa.fa_decode(q, kc, vc, sl, args.splits, o=o, lse=lse, stream=stream)
+
+    torch.cuda.synchronize(dev)
+    times = []
+    for _ in range(args.iters):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        run()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        times.append(e0.elapsed_time(e1))
+    fa.fa_check_device_error(stream)
+    print(f"{args.workload} B={B}: " + " ".join(f"{t:.3f}ms" for t in times))
+
+
+if __name__ == "__main__":
+    main()
