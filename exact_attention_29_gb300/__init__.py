@@ -15,6 +15,7 @@ from ._lib import (  # noqa: F401
     FaError,
     fa_check_device_error,
     fa_decode,
+    fa_decode_noalloc,
     fa_fwd,
     fa_fwd_plan,
     fa_selftest_mma,

@@ -31,6 +31,7 @@ _I = ctypes.c_int
 _SIGNATURES = {
     "fa_fwd": ([_VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, ctypes.c_float, _VP], _I),
     "fa_decode": ([_VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _VP], _I),
+    "fa_decode_noalloc": ([_VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _VP], _I),
     "fa_status_string": ([_I], ctypes.c_char_p),
     "fa_last_error_string": ([], ctypes.c_char_p),
     "fa_check_device_error": ([_VP, ctypes.POINTER(_I)], _I),
@@ -142,6 +143,43 @@ def fa_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, seq
     st = lib.fa_decode(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), seqlens.data_ptr(), o.data_ptr(),
                        lse.data_ptr(), B, H, L, d, int(num_splits), _stream_handle(stream))
     _check(st, "fa_decode")
+    return o, lse
+
+
+NOALLOC_WORKSPACE_FLOATS = 1 << 22
+
+
+def fa_decode_noalloc(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, seqlens: torch.Tensor,
+                      num_splits: int, o: torch.Tensor | None = None, lse: torch.Tensor | None = None, stream=None):
+    """Flash-Decoding that allocates no device memory inside the call.
+
+    Same arguments and results as ``fa_decode``; the split partials go to a
+    fixed 16 MiB array owned by libfa.so instead of a per-call allocation, for
+    callers that cannot allocate while decoding (a serving engine whose KV-cache
+    pool owns nearly all device memory, or a latency-critical loop). Requires
+    B * H * num_splits * (d + 1) <= 4,194,304; all calls share the array, so
+    calls must not overlap on the GPU. Pass ``o`` and ``lse`` to avoid torch
+    allocating the outputs.
+    """
+    lib = load_library()
+    _require(q, "q", torch.bfloat16, 3)
+    _require(k_cache, "k_cache", torch.bfloat16, 4)
+    _require(v_cache, "v_cache", torch.bfloat16, 4)
+    _require(seqlens, "seqlens", torch.int32, 1)
+    B, H, L, d = k_cache.shape
+    if v_cache.shape != k_cache.shape or q.shape != (B, H, d) or seqlens.shape != (B,):
+        raise ValueError("shapes must be q [B,H,d], caches [B,H,L,d], seqlens [B]")
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H), dtype=torch.float32, device=q.device)
+    _require(o, "o", torch.bfloat16, 3)
+    _require(lse, "lse", torch.float32, 2)
+    st = lib.fa_decode_noalloc(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), seqlens.data_ptr(),
+                               o.data_ptr(), lse.data_ptr(), B, H, L, d, int(num_splits), _stream_handle(stream))
+    if st == FA_ERR_INVALID_ARG:
+        raise FaError(st, "fa_decode_noalloc: " + lib.fa_last_error_string().decode())
+    _check(st, "fa_decode_noalloc")
     return o, lse
 
 

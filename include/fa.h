@@ -93,6 +93,32 @@ fa_status fa_fwd(const void *q, const void *k, const void *v, void *o, float *ls
 fa_status fa_decode(const void *q, const void *k_cache, const void *v_cache, const int32_t *seqlens, void *o,
                     float *lse, int B, int H, int L, int d, int num_splits, fa_stream_t stream);
 
+/*
+ * Decode attention that allocates nothing.
+ *
+ * The pages have no counterpart of this call; it exists for callers that
+ * cannot allocate device memory when they decode: a serving engine that gives
+ * nearly all of HBM to its own KV-cache pool at start-up and forbids later
+ * allocations, or a latency-critical decode loop where an allocation could
+ * stall on the pool or fail under fragmentation.
+ *
+ * Arguments, layouts, results and errors are those of fa_decode. The split
+ * partials live in one fixed 16 MiB array of device memory owned by libfa.so
+ * (every GPU that loads the library holds it until the process exits)
+ * instead of a per-call cudaMallocAsync buffer; the call never allocates.
+ *   - Limit: B * H * num_splits * (d + 1) <= 4,194,304 (fp32 values). Larger
+ *     requests return FA_ERR_INVALID_ARG and fa_last_error_string() says why.
+ *   - All calls on a device share the array, which keeps the last call's
+ *     contents; nothing in it needs to start at zero (every partial is written
+ *     before it is read). Calls that may run at the same time on the GPU
+ *     (unordered streams) race on it: order them on one stream.
+ *   - The first call on each device looks up the array's address with that
+ *     device current and caches it; make that first call before any stream
+ *     capture.
+ */
+fa_status fa_decode_noalloc(const void *q, const void *k_cache, const void *v_cache, const int32_t *seqlens,
+                            void *o, float *lse, int B, int H, int L, int d, int num_splits, fa_stream_t stream);
+
 /* Static text for a status code. Never NULL. */
 const char *fa_status_string(fa_status status);
 
