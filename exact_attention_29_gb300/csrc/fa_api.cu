@@ -26,6 +26,7 @@ thread_local char t_error_text[512] = "";
 std::mutex g_mutex;
 unsigned int* g_err_ptr[kMaxDevices] = {};
 int g_dev_ok[kMaxDevices] = {};  // 0 unknown, 1 sm_103, -1 other
+int g_num_sms[kMaxDevices] = {};
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                    const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
@@ -56,6 +57,13 @@ fa_status current_device(int* dev_out) {
       set_error_text("cudaDeviceGetAttribute", e);
       return FA_ERR_CUDA;
     }
+    int sms = 0;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) {
+      set_error_text("cudaDeviceGetAttribute(multiProcessorCount)", e);
+      return FA_ERR_CUDA;
+    }
+    g_num_sms[dev] = sms;
     g_dev_ok[dev] = (major == 10 && minor == 3) ? 1 : -1;
   }
   if (g_dev_ok[dev] != 1) {
@@ -160,7 +168,8 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
   if (st != FA_OK) return st;
   unsigned int* err = device_error_word();
   if (!err) return FA_ERR_CUDA;
-  return launch_fwd(q, k, v, o, lse, B, H, N, d, causal, scale, reinterpret_cast<cudaStream_t>(stream), err);
+  return launch_fwd(q, k, v, o, lse, B, H, N, d, causal, scale, reinterpret_cast<cudaStream_t>(stream), err,
+                    g_num_sms[dev]);
 }
 
 fa_status fa_decode(const void* q, const void* k_cache, const void* v_cache, const int32_t* seqlens, void* o,

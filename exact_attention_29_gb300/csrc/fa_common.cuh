@@ -26,6 +26,8 @@ enum WaitSite : int {
   kSitePFull = 5,
   kSiteOFull = 6,
   kSiteDrain = 7,
+  kSiteQEmpty = 8,
+  kSiteOEmpty = 9,
   kSiteSelftest = 100,
 };
 

@@ -1,5 +1,6 @@
 // Fused prefill attention for sm_103a: tcgen05 tensor cores with TMEM
-// accumulators, TMA-fed shared-memory pipeline, warp-specialised roles.
+// accumulators, TMA-fed shared-memory pipeline, warp-specialised roles,
+// persistent CTAs.
 //
 // What is computed (per (batch, head), FlashAttention-2 order):
 //   "已有的几种大模型上下文支持情况" (cicada blog) §3.2 and CMU 15-779
@@ -13,21 +14,26 @@
 //   than a slack tau); the result stays exact because l and the output
 //   share the same stale base and the final O / l and L use it consistently.
 //
-// Mapping onto one CTA (one SM; TMEM holds 512 columns x 128 lanes):
-//   * two Q tiles of 128 rows each (256 query rows of one head);
+// Mapping onto one CTA (one per SM; TMEM holds 512 columns x 128 lanes):
+//   * a work item is two Q tiles of 128 rows each (256 query rows of one
+//     head); the CTA loops over work items (persistent), so the next item's
+//     Q/K loads and first products overlap the current item's epilogue;
+//   * items are ordered heaviest first (causal: largest row index first) and
+//     dealt to the CTAs in a snake order, which balances the causal load;
 //   * warps 0-3: softmax of Q tile 0, warps 4-7: softmax of Q tile 1
 //     (thread r of a warpgroup owns row r; a row's max and sum are in-thread);
 //   * warp 8: one thread issues every tcgen05.mma and commit;
-//   * warp 9: one thread issues every TMA copy (Q once, then K_j, V_j into a
-//     ring of shared-memory slots).
+//   * warp 9: one thread issues every TMA copy (Q, then K_j, V_j into a ring
+//     of shared-memory slots).
 //   TMEM columns: S0 [0,128), S1 [128,256), O0 [256,256+D), O1 [256+D,256+2D).
 //   P (bf16 pairs) overwrites the first 64 columns of its S tile and is the
 //   TMEM A operand of O += P V. While warpgroup 0 runs the softmax of S0 the
 //   tensor core works on tile 1's products, and the other way round.
 //
-// Every wait is bounded (fa_common.cuh); a wait that runs out records the
-// site, raises the CTA abort flag, and every role drains its in-flight copies
-// or products before TMEM is freed.
+// Every role walks the same item sequence and keeps its own barrier phase
+// counters. Every wait is bounded (fa_common.cuh); a wait that runs out
+// records the site, raises the CTA abort flag, and every role drains its
+// in-flight copies or products before TMEM is freed.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -58,7 +64,8 @@ struct Cfg {
   static constexpr uint32_t kTmemCols = 512;
   static constexpr int kRingOff = 2 * kTileBytes;
   static constexpr int kBarOff = kRingOff + kStages * kTileBytes;
-  static constexpr int kNumBars = 2 + 2 * kStages + 2 + 2 + 2 + 1;
+  // q_full, q_empty, s_full, p_full, o_full, o_empty (2 each), kv_full, kv_empty, mma_done
+  static constexpr int kNumBars = 12 + 2 * kStages + 1;
   static constexpr int kSmemBytes = kBarOff + kNumBars * 8 + 16 + 1024;  // + slack to align to 1 KB
 };
 
@@ -67,7 +74,9 @@ struct FwdParams {
   float* lse;
   unsigned int* err;
   int N;
-  int num_pairs;
+  int BH;          // batch * heads
+  int num_pairs;   // Q-tile pairs per head
+  int num_items;   // BH * num_pairs
   int causal;
   float scale_log2;  // scale * log2(e)
 };
@@ -76,11 +85,13 @@ struct Smem {
   uint8_t* q[2];
   uint8_t* ring;
   uint64_t* q_full;    // [2]   Q tile landed
+  uint64_t* q_empty;   // [2]   last S = Q K^T of an item done: Q buffer free
+  uint64_t* s_full;    // [2]   S = Q K^T done (also: every earlier product done)
+  uint64_t* p_full;    // [2]   P written to TMEM and O rescaled (128 arrivals)
+  uint64_t* o_full;    // [2]   last O += P V of an item done
+  uint64_t* o_empty;   // [2]   O read out of TMEM by the epilogue (128 arrivals)
   uint64_t* kv_full;   // [S]   K or V tile landed in a ring slot
   uint64_t* kv_empty;  // [S]   ring slot free again (committed by the MMA thread)
-  uint64_t* s_full;    // [2]   S = Q K^T done (also: every earlier product of that tile done)
-  uint64_t* p_full;    // [2]   P written to TMEM and O rescaled (128 arrivals)
-  uint64_t* o_full;    // [2]   last O += P V done
   uint64_t* mma_done;  // [1]   every product done (teardown)
   uint32_t* tmem_slot;
   volatile int* abort_flag;
@@ -97,226 +108,327 @@ __device__ __forceinline__ Smem carve(uint8_t* raw) {
   s.ring = base + C::kRingOff;
   uint64_t* bars = reinterpret_cast<uint64_t*>(base + C::kBarOff);
   s.q_full = bars;
-  s.kv_full = bars + 2;
+  s.q_empty = bars + 2;
+  s.s_full = bars + 4;
+  s.p_full = bars + 6;
+  s.o_full = bars + 8;
+  s.o_empty = bars + 10;
+  s.kv_full = bars + 12;
   s.kv_empty = s.kv_full + C::kStages;
-  s.s_full = s.kv_empty + C::kStages;
-  s.p_full = s.s_full + 2;
-  s.o_full = s.p_full + 2;
-  s.mma_done = s.o_full + 2;
+  s.mma_done = s.kv_empty + C::kStages;
   s.tmem_slot = reinterpret_cast<uint32_t*>(s.mma_done + 1);
   s.abort_flag = reinterpret_cast<volatile int*>(s.tmem_slot + 1);
   return s;
 }
 
+// One work item: Q rows [q0, q0 + 256) of head bh; tile t visits n(t) K/V tiles.
+struct Item {
+  int bh;
+  int q0;
+  int n0;
+  int n1;
+  __device__ __forceinline__ int n(int t) const { return t ? n1 : n0; }
+  __device__ __forceinline__ int n_max() const { return n0 > n1 ? n0 : n1; }
+};
+
+// k-th item of this CTA (snake order over the heavy-first item list), or false.
+__device__ __forceinline__ bool item_at(const FwdParams& p, int k, Item& it) {
+  const int G = static_cast<int>(gridDim.x);
+  const int c = static_cast<int>(blockIdx.x);
+  const long long w = static_cast<long long>(k) * G + ((k & 1) ? (G - 1 - c) : c);
+  if (w >= p.num_items) return false;
+  const int rank = static_cast<int>(w / p.BH);
+  it.bh = static_cast<int>(w - static_cast<long long>(rank) * p.BH);
+  const int pair = p.causal ? (p.num_pairs - 1 - rank) : rank;
+  it.q0 = pair * 2 * kBM;
+  it.n0 = fwd_kv_tiles(it.q0, p.N, kBN, p.causal);
+  it.n1 = fwd_kv_tiles(it.q0 + kBM, p.N, kBN, p.causal);
+  return true;
+}
+
 // ---------------------------------------------------------------- TMA producer (one thread)
 template <int D>
 __device__ void load_role(const CUtensorMap* tm_q, const CUtensorMap* tm_k, const CUtensorMap* tm_v, const Smem& sm,
-                          unsigned int* err, int bh, int q0, const int (&n_kv)[2], int n_max) {
+                          const FwdParams& p) {
   using C = Cfg<D>;
   tma_prefetch_desc(tm_q);
   tma_prefetch_desc(tm_k);
   tma_prefetch_desc(tm_v);
-  for (int t = 0; t < 2; ++t) {
-    if (n_kv[t] == 0) continue;
-    mbar_arrive_expect_tx(&sm.q_full[t], C::kTileBytes);
-#pragma unroll
-    for (int c = 0; c < C::kChunks; ++c)
-      tma_load_3d(sm.q[t] + c * kChunkBytes, tm_q, &sm.q_full[t], c * 64, q0 + t * kBM, bh);
-  }
-  int item = 0;  // K_j is item 2j, V_j is item 2j+1
+  uint32_t ring = 0;            // K/V tiles issued so far
+  uint32_t q_cnt[2] = {0, 0};   // Q tiles issued per buffer
   bool ok = true;
-  for (int j = 0; j < n_max && ok; ++j) {
-    for (int kind = 0; kind < 2; ++kind) {
-      const int slot = item % C::kStages;
-      const int use = item / C::kStages;
-      if (use > 0) {
-        ok = bounded_wait(&sm.kv_empty[slot], (use - 1) & 1, sm.abort_flag, err, kSiteKvEmpty);
+  Item it;
+  for (int k = 0; ok && item_at(p, k, it); ++k) {
+    for (int t = 0; t < 2 && ok; ++t) {
+      if (it.n(t) == 0) continue;
+      if (q_cnt[t] > 0) {
+        ok = bounded_wait(&sm.q_empty[t], (q_cnt[t] - 1) & 1, sm.abort_flag, p.err, kSiteQEmpty);
         if (!ok) break;
       }
-      uint8_t* dst = sm.ring + slot * C::kTileBytes;
-      mbar_arrive_expect_tx(&sm.kv_full[slot], C::kTileBytes);
-      const CUtensorMap* map = kind ? tm_v : tm_k;
+      mbar_arrive_expect_tx(&sm.q_full[t], C::kTileBytes);
 #pragma unroll
       for (int c = 0; c < C::kChunks; ++c)
-        tma_load_3d(dst + c * kChunkBytes, map, &sm.kv_full[slot], c * 64, j * kBN, bh);
-      ++item;
+        tma_load_3d(sm.q[t] + c * kChunkBytes, tm_q, &sm.q_full[t], c * 64, it.q0 + t * kBM, it.bh);
+      ++q_cnt[t];
+    }
+    const int n_max = it.n_max();
+    for (int j = 0; j < n_max && ok; ++j) {
+      for (int kind = 0; kind < 2; ++kind) {
+        const uint32_t slot = ring % C::kStages;
+        const uint32_t use = ring / C::kStages;
+        if (use > 0) {
+          ok = bounded_wait(&sm.kv_empty[slot], (use - 1) & 1, sm.abort_flag, p.err, kSiteKvEmpty);
+          if (!ok) break;
+        }
+        uint8_t* dst = sm.ring + slot * C::kTileBytes;
+        mbar_arrive_expect_tx(&sm.kv_full[slot], C::kTileBytes);
+        const CUtensorMap* map = kind ? tm_v : tm_k;
+#pragma unroll
+        for (int c = 0; c < C::kChunks; ++c)
+          tma_load_3d(dst + c * kChunkBytes, map, &sm.kv_full[slot], c * 64, j * kBN, it.bh);
+        ++ring;
+      }
     }
   }
   // Drain: every copy issued must land before the CTA can exit.
-  for (int it = (item > C::kStages ? item - C::kStages : 0); it < item; ++it)
-    bounded_wait(&sm.kv_full[it % C::kStages], (it / C::kStages) & 1, nullptr, err, kSiteDrain);
+  for (uint32_t r = (ring > C::kStages ? ring - C::kStages : 0); r < ring; ++r)
+    bounded_wait(&sm.kv_full[r % C::kStages], (r / C::kStages) & 1, nullptr, p.err, kSiteDrain);
   for (int t = 0; t < 2; ++t)
-    if (n_kv[t] > 0) bounded_wait(&sm.q_full[t], 0, nullptr, err, kSiteDrain);
+    if (q_cnt[t] > 0) bounded_wait(&sm.q_full[t], (q_cnt[t] - 1) & 1, nullptr, p.err, kSiteDrain);
 }
 
 // ---------------------------------------------------------------- MMA issuer (one thread)
 template <int D>
-__device__ void mma_role(const Smem& sm, uint32_t tmem, unsigned int* err, const int (&n_kv)[2], int n_max) {
+__device__ void mma_role(const Smem& sm, uint32_t tmem, const FwdParams& p) {
   using C = Cfg<D>;
-  const uint32_t ring = smem_u32(sm.ring);
-  const uint32_t qa[2] = {smem_u32(sm.q[0]), smem_u32(sm.q[1])};
-  auto slot_addr = [&](int item) { return ring + static_cast<uint32_t>((item % C::kStages) * C::kTileBytes); };
-  auto wait_item = [&](int item) {
-    return bounded_wait(&sm.kv_full[item % C::kStages], (item / C::kStages) & 1, sm.abort_flag, err, kSiteKvFull);
+  const uint32_t ring_base = smem_u32(sm.ring);
+  const uint32_t qa0 = smem_u32(sm.q[0]);
+  const uint32_t qa1 = smem_u32(sm.q[1]);
+  auto slot_addr = [&](uint32_t r) { return ring_base + (r % C::kStages) * static_cast<uint32_t>(C::kTileBytes); };
+  auto wait_kv = [&](uint32_t r) {
+    return bounded_wait(&sm.kv_full[r % C::kStages], (r / C::kStages) & 1, sm.abort_flag, p.err, kSiteKvFull);
   };
-
+  uint32_t ring = 0;                 // K/V tiles consumed so far
+  uint32_t q_cnt[2] = {0, 0};        // Q tiles consumed per buffer
+  uint32_t p_cnt[2] = {0, 0};        // p_full phases consumed per tile
+  uint32_t o_cnt[2] = {0, 0};        // items whose O_t was produced
   bool ok = true;
-  for (int t = 0; t < 2 && ok; ++t)
-    if (n_kv[t] > 0) ok = bounded_wait(&sm.q_full[t], 0, sm.abort_flag, err, kSiteQFull);
-  if (ok) ok = wait_item(0);
-  if (ok) {
+  Item it;
+  for (int k = 0; ok && item_at(p, k, it); ++k) {
+    for (int t = 0; t < 2 && ok; ++t) {
+      if (it.n(t) == 0) continue;
+      ok = bounded_wait(&sm.q_full[t], q_cnt[t] & 1, sm.abort_flag, p.err, kSiteQFull);
+      ++q_cnt[t];
+    }
+    if (!ok) break;
+    const uint32_t base = ring;  // K_j is base + 2j, V_j is base + 2j + 1
+    const int n_max = it.n_max();
+    ok = wait_kv(base);
+    if (!ok) break;
     tc_fence_after();
     for (int t = 0; t < 2; ++t) {
-      if (n_kv[t] == 0) continue;
-      issue_qk<D>(tmem + C::s_col(t), qa[t], slot_addr(0));
+      if (it.n(t) == 0) continue;
+      issue_qk<D>(tmem + C::s_col(t), t ? qa1 : qa0, slot_addr(base));
       umma_commit(&sm.s_full[t]);
+      if (it.n(t) == 1) umma_commit(&sm.q_empty[t]);  // that was this item's last S of tile t
     }
-    umma_commit(&sm.kv_empty[0]);
-  }
-  for (int j = 0; j < n_max && ok; ++j) {
-    const int iv = 2 * j + 1;  // V_j
-    const int ik = 2 * j + 2;  // K_{j+1}
-    ok = wait_item(iv);
-    if (!ok) break;
-    bool k_next = false;
-    for (int t = 0; t < 2; ++t) {
-      if (j >= n_kv[t]) continue;
-      ok = bounded_wait(&sm.p_full[t], j & 1, sm.abort_flag, err, kSitePFull);
+    umma_commit(&sm.kv_empty[base % C::kStages]);
+    for (int j = 0; j < n_max && ok; ++j) {
+      const uint32_t iv = base + 2 * j + 1;  // V_j
+      const uint32_t ik = base + 2 * j + 2;  // K_{j+1}
+      ok = wait_kv(iv);
       if (!ok) break;
-      tc_fence_after();
-      issue_pv<D>(tmem + C::o_col(t), tmem + C::s_col(t), slot_addr(iv), j > 0);
-      if (j + 1 < n_kv[t]) {
-        if (!k_next) {
-          ok = wait_item(ik);
+      bool k_next = false;
+      for (int t = 0; t < 2; ++t) {
+        const int nt = it.n(t);
+        if (j >= nt) continue;
+        ok = bounded_wait(&sm.p_full[t], p_cnt[t] & 1, sm.abort_flag, p.err, kSitePFull);
+        ++p_cnt[t];
+        if (!ok) break;
+        if (j == 0 && o_cnt[t] > 0) {
+          // the first O += P V of an item overwrites O_t: the previous item's
+          // epilogue must have read it out
+          ok = bounded_wait(&sm.o_empty[t], (o_cnt[t] - 1) & 1, sm.abort_flag, p.err, kSiteOEmpty);
           if (!ok) break;
-          tc_fence_after();
-          k_next = true;
         }
-        // issued after P V of the same tile: the tensor pipe runs them in order,
-        // so P is read before the new S overwrites those columns
-        issue_qk<D>(tmem + C::s_col(t), qa[t], slot_addr(ik));
-        umma_commit(&sm.s_full[t]);
-      } else {
-        umma_commit(&sm.o_full[t]);
+        tc_fence_after();
+        issue_pv<D>(tmem + C::o_col(t), tmem + C::s_col(t), slot_addr(iv), j > 0);
+        if (j + 1 < nt) {
+          if (!k_next) {
+            ok = wait_kv(ik);
+            if (!ok) break;
+            tc_fence_after();
+            k_next = true;
+          }
+          // issued after P V of the same tile: the tensor pipe runs them in order,
+          // so P is read before the new S overwrites those columns
+          issue_qk<D>(tmem + C::s_col(t), t ? qa1 : qa0, slot_addr(ik));
+          umma_commit(&sm.s_full[t]);
+          if (j + 2 == nt) umma_commit(&sm.q_empty[t]);
+        } else {
+          umma_commit(&sm.o_full[t]);
+          ++o_cnt[t];
+        }
       }
+      if (!ok) break;
+      umma_commit(&sm.kv_empty[iv % C::kStages]);
+      if (k_next) umma_commit(&sm.kv_empty[ik % C::kStages]);
     }
-    if (!ok) break;
-    umma_commit(&sm.kv_empty[iv % C::kStages]);
-    if (k_next) umma_commit(&sm.kv_empty[ik % C::kStages]);
+    ring = base + 2 * n_max;
   }
   // Teardown: every product issued so far must finish before TMEM is freed.
   umma_commit(sm.mma_done);
-  bounded_wait(sm.mma_done, 0, nullptr, err, kSiteDrain);
+  bounded_wait(sm.mma_done, 0, nullptr, p.err, kSiteDrain);
 }
 
 // ---------------------------------------------------------------- softmax + epilogue (128 threads per tile)
 template <int D>
-__device__ void softmax_role(const Smem& sm, uint32_t tmem, const FwdParams& p, int warp, int lane, int bh, int q0,
-                             const int (&n_kv)[2]) {
+__device__ void softmax_role(const Smem& sm, uint32_t tmem, const FwdParams& p, int warp, int lane) {
   using C = Cfg<D>;
   const int t = warp >> 2;
   const int quarter = warp & 3;  // this warp may touch TMEM lanes [32*quarter, 32*quarter+32)
   const int row = quarter * 32 + lane;
-  const int q_row = q0 + t * kBM + row;
-  const int nkv = n_kv[t];
-  if (nkv == 0) return;
   const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
   const uint32_t s_tm = tmem + lane_base + C::s_col(t);
   const uint32_t o_tm = tmem + lane_base + C::o_col(t);
   const float sl2 = p.scale_log2;
-  const int vis_end = p.causal ? min(q_row + 1, p.N) : p.N;  // keys [0, vis_end) are visible to this row
-
-  float m_used = -INFINITY;  // base of every exponent so far (log2 domain, scaled)
-  float l = 0.f;
+  const uint64_t sl2x2 = f2_pack(sl2, sl2);
+  uint32_t s_cnt = 0;  // s_full phases consumed
+  uint32_t o_cnt = 0;  // o_full phases consumed
   bool ok = true;
-  for (int j = 0; j < nkv; ++j) {
-    ok = bounded_wait(&sm.s_full[t], j & 1, sm.abort_flag, p.err, kSiteSFull);
+  Item it;
+  for (int k = 0; ok && item_at(p, k, it); ++k) {
+    const int nkv = it.n(t);
+    if (nkv == 0) continue;
+    const int q_row = it.q0 + t * kBM + row;
+    const int vis_end = p.causal ? min(q_row + 1, p.N) : p.N;  // keys [0, vis_end) are visible to this row
+    float m_used = -INFINITY;  // base of every exponent so far (log2 domain, scaled)
+    float l = 0.f;
+    for (int j = 0; j < nkv; ++j) {
+      ok = bounded_wait(&sm.s_full[t], s_cnt & 1, sm.abort_flag, p.err, kSiteSFull);
+      ++s_cnt;
+      ok = __all_sync(kFull, ok);
+      if (!ok) break;
+      tc_fence_after();
+
+      // Pass 1: row maximum of the raw scores, 64 columns at a time (scale > 0,
+      // so the maximum commutes with the scaling).
+      const int lim = vis_end - j * kBN;  // visible keys of this tile for this row
+      float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        uint32_t r[64];
+        tmem_ld_x64(s_tm + 64 * h, r);
+        if (lim < kBN) {
+#pragma unroll
+          for (int c = 0; c < 64; ++c)
+            if (64 * h + c >= lim) r[c] = 0xff800000u;  // -inf
+        }
+#pragma unroll
+        for (int c = 0; c < 64; c += 8) {
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            mx[i] = fmax3(mx[i], __uint_as_float(r[c + 2 * i]), __uint_as_float(r[c + 2 * i + 1]));
+        }
+      }
+      const float m_tile = fmax3(fmaxf(mx[0], mx[1]), mx[2], mx[3]) * sl2;
+
+      const bool need = (m_used != -INFINITY) && (m_tile > m_used + kRescaleSlack);
+      if (__any_sync(kFull, need)) {
+        const float alpha = need ? ex2_approx(m_used - m_tile) : 1.f;
+        if (need) {
+          l *= alpha;
+          m_used = m_tile;
+        }
+        const uint64_t alpha2 = f2_pack(alpha, alpha);
+#pragma unroll 1
+        for (int c = 0; c < D; c += 32) {
+          uint32_t r[32];
+          tmem_ld_x32(o_tm + c, r);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            float lo, hi;
+            f2_unpack(f2_mul(f2_pack(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1])), alpha2), lo, hi);
+            r[2 * i] = __float_as_uint(lo);
+            r[2 * i + 1] = __float_as_uint(hi);
+          }
+          tmem_st_x32(o_tm + c, r);
+        }
+      }
+      if (m_used == -INFINITY) m_used = m_tile;  // first visible scores of this row
+      const float m_sub = (m_used == -INFINITY) ? 0.f : m_used;
+
+      // Pass 2: p = 2^(s * scale * log2 e - m), two at a time, row sum in
+      // packed pairs; the bf16 pairs of keys [64h, 64h + 64) go to P columns
+      // [32h, 32h + 32), which only hold scores this pass has already read.
+      const uint64_t negm2 = f2_pack(-m_sub, -m_sub);
+      uint64_t acc[4] = {0, 0, 0, 0};
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        uint32_t r[64];
+        tmem_ld_x64(s_tm + 64 * h, r);
+        if (lim < kBN) {
+#pragma unroll
+          for (int c = 0; c < 64; ++c)
+            if (64 * h + c >= lim) r[c] = 0xff800000u;
+        }
+        // x = s * scale_log2 - m in place, then 2^x in place (MUFU), then pack + sum
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          float x0, x1;
+          f2_unpack(f2_fma(f2_pack(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1])), sl2x2, negm2), x0, x1);
+          r[2 * i] = __float_as_uint(ex2_approx(x0));
+          r[2 * i + 1] = __float_as_uint(ex2_approx(x1));
+        }
+        uint32_t pk[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const float p0 = __uint_as_float(r[2 * i]);
+          const float p1 = __uint_as_float(r[2 * i + 1]);
+          acc[i & 3] = f2_add(acc[i & 3], f2_pack(p0, p1));
+          pk[i] = pack_bf16x2(p0, p1);
+        }
+        tmem_st_x32(s_tm + 32 * h, pk);
+      }
+      float s0, s1, s2, s3;
+      f2_unpack(f2_add(acc[0], acc[1]), s0, s1);
+      f2_unpack(f2_add(acc[2], acc[3]), s2, s3);
+      l += (s0 + s1) + (s2 + s3);
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(&sm.p_full[t]);
+    }
+    if (!ok) break;
+    ok = bounded_wait(&sm.o_full[t], o_cnt & 1, sm.abort_flag, p.err, kSiteOFull);
+    ++o_cnt;
     ok = __all_sync(kFull, ok);
     if (!ok) break;
     tc_fence_after();
 
-    uint32_t ra[64], rb[64];
-    tmem_ld_x64(s_tm, ra);
-    tmem_ld_x64(s_tm + 64, rb);
-    float s[128];
+    // Epilogue: O / l to bf16 in registers, release O's TMEM columns, then store.
+    const float inv_l = 1.f / l;
+    const uint64_t inv_l2 = f2_pack(inv_l, inv_l);
+    uint32_t w[D / 2];
 #pragma unroll
-    for (int c = 0; c < 64; ++c) {
-      s[c] = __uint_as_float(ra[c]);
-      s[64 + c] = __uint_as_float(rb[c]);
-    }
-    const int lim = vis_end - j * kBN;  // visible keys of this tile for this row
-    if (lim < kBN) {
+    for (int c = 0; c < D; c += 32) {
+      uint32_t r[32];
+      tmem_ld_x32(o_tm + c, r);
 #pragma unroll
-      for (int c = 0; c < 128; ++c)
-        if (c >= lim) s[c] = -INFINITY;
-    }
-    float mx[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) mx[i] = s[i];
-#pragma unroll
-    for (int c = 8; c < 128; ++c) mx[c & 7] = fmaxf(mx[c & 7], s[c]);
-    const float m_tile = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                               fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * sl2;
-
-    const bool need = (m_used != -INFINITY) && (m_tile > m_used + kRescaleSlack);
-    if (__any_sync(kFull, need)) {
-      const float alpha = need ? ex2_approx(m_used - m_tile) : 1.f;
-      if (need) {
-        l *= alpha;
-        m_used = m_tile;
-      }
-#pragma unroll 1
-      for (int c = 0; c < D; c += 32) {
-        uint32_t r[32];
-        tmem_ld_x32(o_tm + c, r);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
-        tmem_st_x32(o_tm + c, r);
+      for (int i = 0; i < 16; ++i) {
+        float lo, hi;
+        f2_unpack(f2_mul(f2_pack(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1])), inv_l2), lo, hi);
+        w[c / 2 + i] = pack_bf16x2(lo, hi);
       }
     }
-    if (m_used == -INFINITY) m_used = m_tile;  // first visible scores of this row
-    const float m_sub = (m_used == -INFINITY) ? 0.f : m_used;
-
-    uint32_t pk[64];
-    float sum[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-    for (int i = 0; i < 64; ++i) {
-      const float p0 = ex2_approx(fmaf(s[2 * i], sl2, -m_sub));
-      const float p1 = ex2_approx(fmaf(s[2 * i + 1], sl2, -m_sub));
-      sum[i & 3] += p0 + p1;
-      pk[i] = pack_bf16x2(p0, p1);
-    }
-    l += (sum[0] + sum[1]) + (sum[2] + sum[3]);
-    tmem_st_x64(s_tm, pk);
-    tmem_st_wait();
     tc_fence_before();
-    mbar_arrive(&sm.p_full[t]);
-  }
-  if (ok) {
-    ok = bounded_wait(&sm.o_full[t], 0, sm.abort_flag, p.err, kSiteOFull);
-    ok = __all_sync(kFull, ok);
-  }
-  if (!ok) return;
-  tc_fence_after();
-
-  const float inv_l = 1.f / l;
-  const bool in_range = q_row < p.N;
-  __nv_bfloat16* orow = p.o + (static_cast<size_t>(bh) * p.N + (in_range ? q_row : 0)) * D;
-#pragma unroll 1
-  for (int c = 0; c < D; c += 32) {
-    uint32_t r[32];
-    tmem_ld_x32(o_tm + c, r);
-    uint32_t w[16];
+    mbar_arrive(&sm.o_empty[t]);
+    if (q_row < p.N) {
+      uint4* dst = reinterpret_cast<uint4*>(p.o + (static_cast<size_t>(it.bh) * p.N + q_row) * D);
 #pragma unroll
-    for (int i = 0; i < 16; ++i)
-      w[i] = pack_bf16x2(__uint_as_float(r[2 * i]) * inv_l, __uint_as_float(r[2 * i + 1]) * inv_l);
-    if (in_range) {
-      uint4* dst = reinterpret_cast<uint4*>(orow + c);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+      for (int i = 0; i < D / 8; ++i) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+      p.lse[static_cast<size_t>(it.bh) * p.N + q_row] = (m_used + log2f(l)) * kLn2;
     }
   }
-  if (in_range) p.lse[static_cast<size_t>(bh) * p.N + q_row] = (m_used + log2f(l)) * kLn2;
 }
 
 template <int D>
@@ -328,19 +440,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   const Smem sm = carve<D>(smem_raw);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int bh = blockIdx.x;
-  // causal: launch the heaviest Q-tile pairs (largest row index) first
-  const int pair = p.causal ? (p.num_pairs - 1 - static_cast<int>(blockIdx.y)) : static_cast<int>(blockIdx.y);
-  const int q0 = pair * 2 * kBM;
-  const int n_kv[2] = {fwd_kv_tiles(q0, p.N, kBN, p.causal), fwd_kv_tiles(q0 + kBM, p.N, kBN, p.causal)};
-  const int n_max = max(n_kv[0], n_kv[1]);
 
   if (threadIdx.x == 0) {
     for (int t = 0; t < 2; ++t) {
       mbar_init(&sm.q_full[t], 1);
+      mbar_init(&sm.q_empty[t], 1);
       mbar_init(&sm.s_full[t], 1);
       mbar_init(&sm.p_full[t], 128);
       mbar_init(&sm.o_full[t], 1);
+      mbar_init(&sm.o_empty[t], 128);
     }
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(&sm.kv_full[s], 1);
@@ -360,11 +468,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *sm.tmem_slot;
 
   if (warp == kLoadWarp) {
-    if (lane == 0) load_role<D>(&tm_q, &tm_k, &tm_v, sm, p.err, bh, q0, n_kv, n_max);
+    if (lane == 0) load_role<D>(&tm_q, &tm_k, &tm_v, sm, p);
   } else if (warp == kMmaWarp) {
-    if (lane == 0) mma_role<D>(sm, tmem, p.err, n_kv, n_max);
+    if (lane == 0) mma_role<D>(sm, tmem, p);
   } else {
-    softmax_role<D>(sm, tmem, p, warp, lane, bh, q0, n_kv);
+    softmax_role<D>(sm, tmem, p, warp, lane);
   }
 
   tc_fence_before();
@@ -378,7 +486,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int D>
 fa_status launch(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int causal,
-                 float scale, cudaStream_t stream, unsigned int* err) {
+                 float scale, cudaStream_t stream, unsigned int* err, int num_sms) {
   using C = Cfg<D>;
   CUtensorMap tq, tk, tv;
   const uint64_t bh = static_cast<uint64_t>(B) * H;
@@ -386,12 +494,15 @@ fa_status launch(const void* q, const void* k, const void* v, void* o, float* ls
       !encode_bf16_map(&tv, v, D, N, bh, kBN))
     return FA_ERR_CUDA;
   const int num_pairs = (N + 2 * kBM - 1) / (2 * kBM);
+  const long long items = static_cast<long long>(bh) * num_pairs;
   FwdParams prm;
   prm.o = static_cast<__nv_bfloat16*>(o);
   prm.lse = lse;
   prm.err = err;
   prm.N = N;
+  prm.BH = static_cast<int>(bh);
   prm.num_pairs = num_pairs;
+  prm.num_items = static_cast<int>(items);
   prm.causal = causal ? 1 : 0;
   prm.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   cudaError_t e = cudaFuncSetAttribute(fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
@@ -399,7 +510,7 @@ fa_status launch(const void* q, const void* k, const void* v, void* o, float* ls
     set_error_text("cudaFuncSetAttribute(fwd_kernel)", e);
     return FA_ERR_CUDA;
   }
-  dim3 grid(static_cast<unsigned>(bh), static_cast<unsigned>(num_pairs));
+  const int grid = static_cast<int>(items < num_sms ? items : num_sms);
   fwd_kernel<D><<<grid, kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, prm);
   e = cudaGetLastError();
   if (e != cudaSuccess) {
@@ -412,9 +523,9 @@ fa_status launch(const void* q, const void* k, const void* v, void* o, float* ls
 }  // namespace
 
 fa_status launch_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
-                     int causal, float scale, cudaStream_t stream, unsigned int* err) {
-  if (d == 128) return launch<128>(q, k, v, o, lse, B, H, N, causal, scale, stream, err);
-  if (d == 64) return launch<64>(q, k, v, o, lse, B, H, N, causal, scale, stream, err);
+                     int causal, float scale, cudaStream_t stream, unsigned int* err, int num_sms) {
+  if (d == 128) return launch<128>(q, k, v, o, lse, B, H, N, causal, scale, stream, err, num_sms);
+  if (d == 64) return launch<64>(q, k, v, o, lse, B, H, N, causal, scale, stream, err, num_sms);
   return FA_ERR_UNSUPPORTED;
 }
 

@@ -22,8 +22,9 @@ void set_error_text(const char* what, const char* detail);
 // Device error word of the current device (see fa_common.cuh).
 unsigned int* device_error_word();
 
+// num_sms: multiprocessor count of the current device (the persistent grid size).
 fa_status launch_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
-                     int causal, float scale, cudaStream_t stream, unsigned int* err);
+                     int causal, float scale, cudaStream_t stream, unsigned int* err, int num_sms);
 
 fa_status launch_decode(const void* q, const void* k_cache, const void* v_cache, const int32_t* seqlens, void* o,
                         float* lse, int B, int H, int L, int d, int num_splits, float* ws_o, float* ws_lse,
