@@ -29,24 +29,20 @@ __device__ __forceinline__ void issue_qk(uint32_t s_tmem, uint32_t q_smem, uint3
   }
 }
 
-// O(tmem, 128 x D fp32) (+)= P(tmem, 128 x 128 bf16, packed pairs) * V(smem, 128 keys x D, MN-major),
-// K-steps [kk0, kk1) of 16 keys each (the full product is kk0 = 0, kk1 = 8).
+// O(tmem, 128 x D fp32) (+)= P(tmem, 128 x 128 bf16, packed pairs) * V(smem, 128 keys x D, MN-major).
+// P keys 0-63 sit in TMEM columns [p, p + 32) and keys 64-127 in
+// [p + 32 + p_gap, p + 64 + p_gap); each K-step of 16 keys takes 8 columns.
 template <int D>
-__device__ __forceinline__ void issue_pv_steps(uint32_t o_tmem, uint32_t p_tmem, uint32_t v_smem, bool accumulate,
-                                               int kk0, int kk1) {
+__device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem, uint32_t v_smem, bool accumulate,
+                                         uint32_t p_gap = 0) {
   constexpr uint32_t idesc = idesc_bf16_f32(kBM, D, false, true);
 #pragma unroll
-  for (int kk = kk0; kk < kk1; ++kk) {
-    // 16 keys = two 8-row groups of 1024 bytes; P advances 8 packed columns
-    umma_ts(o_tmem, p_tmem + static_cast<uint32_t>(kk * 8),
+  for (int kk = 0; kk < kBN / 16; ++kk) {
+    // 16 keys = two 8-row groups of 1024 bytes of V
+    umma_ts(o_tmem, p_tmem + static_cast<uint32_t>(kk * 8) + (kk >= 4 ? p_gap : 0u),
             smem_desc_sw128(v_smem + static_cast<uint32_t>(kk * 2048), kChunkBytes, 1024), idesc,
             (accumulate || kk > 0) ? 1u : 0u);
   }
-}
-
-template <int D>
-__device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem, uint32_t v_smem, bool accumulate) {
-  issue_pv_steps<D>(o_tmem, p_tmem, v_smem, accumulate, 0, kBN / 16);
 }
 
 }  // namespace fa
