@@ -85,13 +85,13 @@ struct Smem {
   uint8_t* q[2];
   uint8_t* ring;
   uint64_t* q_full;    // [2]   Q tile landed
-  uint64_t* q_empty;   // [2]   last S = Q K^T of an item done: Q buffer free
+  uint64_t* q_empty;   // [2]   last S = Q K^T of an item done: Q buffer free (softmax arrives)
   uint64_t* s_full;    // [2]   S = Q K^T done (also: every earlier product done)
   uint64_t* p_full;    // [2]   P written to TMEM and O rescaled (128 arrivals)
   uint64_t* o_full;    // [2]   last O += P V of an item done
   uint64_t* o_empty;   // [2]   O read out of TMEM by the epilogue (128 arrivals)
   uint64_t* kv_full;   // [S]   K or V tile landed in a ring slot
-  uint64_t* kv_empty;  // [S]   ring slot free again (committed by the MMA thread)
+  uint64_t* kv_empty;  // [S]   ring slot free again (softmax arrives)
   uint64_t* mma_done;  // [1]   every product done (teardown)
   uint32_t* tmem_slot;
   volatile int* abort_flag;
@@ -230,9 +230,7 @@ __device__ void mma_role(const Smem& sm, uint32_t tmem, const FwdParams& p) {
       if (it.n(t) == 0) continue;
       issue_qk<D>(tmem + C::s_col(t), t ? qa1 : qa0, slot_addr(base));
       umma_commit(&sm.s_full[t]);
-      if (it.n(t) == 1) umma_commit(&sm.q_empty[t]);  // that was this item's last S of tile t
     }
-    umma_commit(&sm.kv_empty[base % C::kStages]);
     for (int j = 0; j < n_max && ok; ++j) {
       const uint32_t iv = base + 2 * j + 1;  // V_j
       const uint32_t ik = base + 2 * j + 2;  // K_{j+1}
@@ -264,21 +262,37 @@ __device__ void mma_role(const Smem& sm, uint32_t tmem, const FwdParams& p) {
           // so P is read before the new S overwrites those columns
           issue_qk<D>(tmem + C::s_col(t), t ? qa1 : qa0, slot_addr(ik));
           umma_commit(&sm.s_full[t]);
-          if (j + 2 == nt) umma_commit(&sm.q_empty[t]);
         } else {
           umma_commit(&sm.o_full[t]);
           ++o_cnt[t];
         }
       }
       if (!ok) break;
-      umma_commit(&sm.kv_empty[iv % C::kStages]);
-      if (k_next) umma_commit(&sm.kv_empty[ik % C::kStages]);
     }
     ring = base + 2 * n_max;
   }
   // Teardown: every product issued so far must finish before TMEM is freed.
   umma_commit(sm.mma_done);
   bounded_wait(sm.mma_done, 0, nullptr, p.err, kSiteDrain);
+}
+
+// The tile whose products read K_j and V_j last (tile 1 unless it stops earlier).
+__device__ __forceinline__ int last_reader(const Item& it, int j) { return (it.n1 > j) ? 1 : 0; }
+
+// Buffer releases, made by one softmax thread per tile with plain mbarrier
+// arrivals right after it has seen S_t(j) complete (a tcgen05.commit for each
+// release would cost tensor-pipe time). S_t(j) done means every product issued
+// before it is done too:
+//   K_j      is free when the S of its last reader is done,
+//   V_(j-1)  is free when the next S of its last reader is done (the last V of
+//            a tile is released after that tile's final O += P V instead),
+//   Q_t      is free when the item's last S_t is done.
+template <int D>
+__device__ __forceinline__ void release_after_s(const Smem& sm, const Item& it, int t, int j, uint32_t ring_base) {
+  using C = Cfg<D>;
+  if (last_reader(it, j) == t) mbar_arrive(&sm.kv_empty[(ring_base + 2 * j) % C::kStages]);
+  if (j > 0 && last_reader(it, j - 1) == t) mbar_arrive(&sm.kv_empty[(ring_base + 2 * (j - 1) + 1) % C::kStages]);
+  if (j == it.n(t) - 1) mbar_arrive(&sm.q_empty[t]);
 }
 
 // ---------------------------------------------------------------- softmax + epilogue (128 threads per tile)
@@ -297,7 +311,11 @@ __device__ void softmax_role(const Smem& sm, uint32_t tmem, const FwdParams& p, 
   uint32_t o_cnt = 0;  // o_full phases consumed
   bool ok = true;
   Item it;
+  const bool releaser = (quarter == 0 && lane == 0);  // one thread per tile releases buffers
+  uint32_t ring_next = 0;                             // K/V ring position of the next item
   for (int k = 0; ok && item_at(p, k, it); ++k) {
+    const uint32_t ring_base = ring_next;  // K_j is ring_base + 2j, V_j is ring_base + 2j + 1
+    ring_next += 2 * it.n_max();
     const int nkv = it.n(t);
     if (nkv == 0) continue;
     const int q_row = it.q0 + t * kBM + row;
@@ -309,6 +327,7 @@ __device__ void softmax_role(const Smem& sm, uint32_t tmem, const FwdParams& p, 
       ++s_cnt;
       ok = __all_sync(kFull, ok);
       if (!ok) break;
+      if (releaser) release_after_s<D>(sm, it, t, j, ring_base);
       tc_fence_after();
 
       // Pass 1: row maximum of the raw scores, 64 columns at a time (scale > 0,
@@ -403,6 +422,9 @@ __device__ void softmax_role(const Smem& sm, uint32_t tmem, const FwdParams& p, 
     ++o_cnt;
     ok = __all_sync(kFull, ok);
     if (!ok) break;
+    // the last P V of this tile is done: its V tile is free if this tile was its last reader
+    if (releaser && last_reader(it, nkv - 1) == t)
+      mbar_arrive(&sm.kv_empty[(ring_base + 2 * (nkv - 1) + 1) % C::kStages]);
     tc_fence_after();
 
     // Epilogue: O / l to bf16 in registers, release O's TMEM columns, then store.
