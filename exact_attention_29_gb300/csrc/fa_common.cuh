@@ -28,7 +28,6 @@ enum WaitSite : int {
   kSiteDrain = 7,
   kSiteQEmpty = 8,
   kSiteOEmpty = 9,
-  kSitePair = 10,
   kSiteSelftest = 100,
 };
 
