@@ -12,6 +12,7 @@ Public functions
 attention(q, k, v, causal, scale)            -> (o, lse), [B,H,N,d] inputs
 attention_rows(q_rows, q_pos, k, v, ...)     -> (o, lse, s, p) for one head
 decode(q, k_cache, v_cache, seqlens)         -> (o, lse), one query per (b, h)
+attention_bwd(q, k, v, dout, causal, scale)  -> (dq, dk, dv), [B,H,N,d] inputs
 
 Inputs may be numpy arrays or torch CPU tensors of any float dtype; they are
 widened to fp64 exactly (bf16 and fp32 values are representable in fp64), so
@@ -67,6 +68,8 @@ def _load():
             lib.oracle_attention.restype = ctypes.c_int
             lib.oracle_decode.argtypes = [dp, dp, dp, ip, dp, dp] + [ctypes.c_int] * 4
             lib.oracle_decode.restype = ctypes.c_int
+            lib.oracle_attention_bwd.argtypes = [dp] * 7 + [ctypes.c_int] * 5 + [ctypes.c_double]
+            lib.oracle_attention_bwd.restype = ctypes.c_int
             _lib = lib
     return _lib
 
@@ -159,3 +162,20 @@ def decode(q, k_cache, v_cache, seqlens):
                            B, H, L, d)
     _check(rc, "decode")
     return o, lse
+
+
+def attention_bwd(q, k, v, dout, causal: bool, scale: float):
+    """Backward of standard attention over [B, H, N, d] tensors.
+
+    Returns (dq, dk, dv) for the upstream gradient dout of O, as fp64 arrays.
+    """
+    lib = _load()
+    qq, kk, vv, gg = _f64(q), _f64(k), _f64(v), _f64(dout)
+    if qq.ndim != 4 or not (qq.shape == kk.shape == vv.shape == gg.shape):
+        raise ValueError("q, k, v, dout must all be [B, H, N, d]")
+    B, H, N, d = qq.shape
+    dq, dk, dv = np.empty_like(qq), np.empty_like(qq), np.empty_like(qq)
+    rc = lib.oracle_attention_bwd(_ptr(qq), _ptr(kk), _ptr(vv), _ptr(gg), _ptr(dq), _ptr(dk), _ptr(dv),
+                                  B, H, N, d, int(bool(causal)), float(scale))
+    _check(rc, "attention_bwd")
+    return dq, dk, dv

@@ -193,3 +193,118 @@ int oracle_decode(const double *q, const double *k_cache, const double *v_cache,
   }
   return ORACLE_OK;
 }
+
+/*
+ * Backward of standard attention for one (batch, head), every intermediate
+ * materialised, fp64.
+ *
+ *   q, k, v, dout  [n][d]; outputs dq, dk, dv [n][d].
+ *
+ * With S' = scale * Q K^T (+ causal -inf), P = softmax(S') row-wise,
+ * O = P V and the upstream gradient dO:
+ *   dV = P^T dO
+ *   dP = dO V^T
+ *   D_i = sum_j P_ij dP_ij            (equal to rowsum(dO_i * O_i))
+ *   dS = P * (dP - D)                 (softmax Jacobian diag(p) - p p^T)
+ *   dQ = scale * dS K,  dK = scale * dS^T Q
+ * Sources: CMU 15-779 Lecture 5 notes §7.1 (the chain rule and the softmax
+ * Jacobian), §7.3 (D_i = dO_i . O_i lets dS be formed block by block);
+ * "FlashAttention 完全拆解（一）", backward section (dS from P, dP and D).
+ * The oracle forms D from its definition sum_j P_ij dP_ij.
+ */
+int oracle_attention_bwd_head(const double *q, const double *k, const double *v,
+                              const double *dout, int n, int d, int causal,
+                              double scale, double *dq, double *dk, double *dv) {
+  if (n < 1 || d < 1) return ORACLE_ERR_ARG;
+  size_t nn = (size_t)n * n;
+  double *P = (double *)malloc(nn * sizeof(double));
+  double *dP = (double *)malloc(nn * sizeof(double));
+  double *Dv = (double *)malloc((size_t)n * sizeof(double));
+  if (!P || !dP || !Dv) {
+    free(P); free(dP); free(Dv);
+    return ORACLE_ERR_NOMEM;
+  }
+  /* P = softmax(scale * Q K^T + mask), row by row (safe softmax). */
+#pragma omp parallel for schedule(static)
+  for (int i = 0; i < n; ++i) {
+    double *Pi = P + (size_t)i * n;
+    double mi = -INFINITY;
+    for (int j = 0; j < n; ++j) {
+      double acc = 0.0;
+      for (int t = 0; t < d; ++t) acc += q[(size_t)i * d + t] * k[(size_t)j * d + t];
+      double x = scale * acc;
+      if (causal && j > i) x = -INFINITY;
+      Pi[j] = x;
+      if (x > mi) mi = x;
+    }
+    double li = 0.0;
+    for (int j = 0; j < n; ++j) {
+      double e = (Pi[j] == -INFINITY) ? 0.0 : exp(Pi[j] - mi);
+      Pi[j] = e;
+      li += e;
+    }
+    for (int j = 0; j < n; ++j) Pi[j] /= li;
+  }
+  /* dP = dO V^T and D_i = sum_j P_ij dP_ij. */
+#pragma omp parallel for schedule(static)
+  for (int i = 0; i < n; ++i) {
+    double Di = 0.0;
+    for (int j = 0; j < n; ++j) {
+      double acc = 0.0;
+      for (int t = 0; t < d; ++t) acc += dout[(size_t)i * d + t] * v[(size_t)j * d + t];
+      dP[(size_t)i * n + j] = acc;
+      Di += P[(size_t)i * n + j] * acc;
+    }
+    Dv[i] = Di;
+  }
+  /* dS = P * (dP - D), kept in dP. */
+#pragma omp parallel for schedule(static)
+  for (int i = 0; i < n; ++i)
+    for (int j = 0; j < n; ++j) {
+      size_t ij = (size_t)i * n + j;
+      dP[ij] = P[ij] * (dP[ij] - Dv[i]);
+    }
+  /* dQ = scale * dS K. */
+#pragma omp parallel for schedule(static)
+  for (int i = 0; i < n; ++i) {
+    for (int t = 0; t < d; ++t) dq[(size_t)i * d + t] = 0.0;
+    for (int j = 0; j < n; ++j) {
+      double s = dP[(size_t)i * n + j];
+      for (int t = 0; t < d; ++t) dq[(size_t)i * d + t] += s * k[(size_t)j * d + t];
+    }
+    for (int t = 0; t < d; ++t) dq[(size_t)i * d + t] *= scale;
+  }
+  /* dK = scale * dS^T Q and dV = P^T dO. */
+#pragma omp parallel for schedule(static)
+  for (int j = 0; j < n; ++j) {
+    for (int t = 0; t < d; ++t) {
+      dk[(size_t)j * d + t] = 0.0;
+      dv[(size_t)j * d + t] = 0.0;
+    }
+    for (int i = 0; i < n; ++i) {
+      double s = dP[(size_t)i * n + j];
+      double p = P[(size_t)i * n + j];
+      for (int t = 0; t < d; ++t) {
+        dk[(size_t)j * d + t] += s * q[(size_t)i * d + t];
+        dv[(size_t)j * d + t] += p * dout[(size_t)i * d + t];
+      }
+    }
+    for (int t = 0; t < d; ++t) dk[(size_t)j * d + t] *= scale;
+  }
+  free(P); free(dP); free(Dv);
+  return ORACLE_OK;
+}
+
+/* Backward over [B][H][N][d] tensors, one head at a time. */
+int oracle_attention_bwd(const double *q, const double *k, const double *v,
+                         const double *dout, double *dq, double *dk, double *dv,
+                         int B, int H, int N, int d, int causal, double scale) {
+  if (B < 1 || H < 1 || N < 1 || d < 1) return ORACLE_ERR_ARG;
+  for (int bh = 0; bh < B * H; ++bh) {
+    size_t off = (size_t)bh * N * d;
+    int rc = oracle_attention_bwd_head(q + off, k + off, v + off, dout + off, N, d,
+                                       causal, scale, dq + off, dk + off, dv + off);
+    if (rc != ORACLE_OK) return rc;
+  }
+  return ORACLE_OK;
+}
