@@ -13,6 +13,8 @@ from ._lib import (  # noqa: F401
     FA_OK,
     LIB_PATH,
     FaError,
+    fa_bwd,
+    fa_bwd_plan,
     fa_check_device_error,
     fa_decode,
     fa_decode_noalloc,

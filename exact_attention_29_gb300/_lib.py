@@ -31,6 +31,8 @@ _I = ctypes.c_int
 _SIGNATURES = {
     "fa_fwd": ([_VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, ctypes.c_float, _VP], _I),
     "fa_decode": ([_VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _VP], _I),
+    "fa_bwd": ([_VP] * 9 + [_I] * 5 + [ctypes.c_float, _VP], _I),
+    "fa_bwd_plan": ([_I, _I, _I, _I, ctypes.POINTER(ctypes.c_longlong)], _I),
     "fa_decode_noalloc": ([_VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _VP], _I),
     "fa_status_string": ([_I], ctypes.c_char_p),
     "fa_last_error_string": ([], ctypes.c_char_p),
@@ -118,6 +120,46 @@ def fa_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = Fal
                     1 if causal else 0, float(scale), _stream_handle(stream))
     _check(st, "fa_fwd")
     return o, lse
+
+
+def fa_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor, lse: torch.Tensor,
+           dout: torch.Tensor, causal: bool = False, scale: float | None = None, dq=None, dk=None, dv=None,
+           stream=None):
+    """Gradients of fa_fwd. q, k, v, o, dout bf16 [B,H,N,d]; lse fp32 [B,H,N] (from fa_fwd).
+
+    Returns (dq, dk, dv), bf16 [B,H,N,d].
+    """
+    lib = load_library()
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (o, "o"), (dout, "dout")):
+        _require(t, n, torch.bfloat16, 4)
+    _require(lse, "lse", torch.float32, 3)
+    if not (k.shape == v.shape == o.shape == dout.shape == q.shape):
+        raise ValueError("q, k, v, o and dout must have the same shape [B, H, N, d]")
+    B, H, N, d = q.shape
+    if lse.shape != (B, H, N):
+        raise ValueError("lse must be [B, H, N]")
+    if scale is None:
+        scale = d ** -0.5
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(q) if dk is None else dk
+    dv = torch.empty_like(q) if dv is None else dv
+    for t, n in ((dq, "dq"), (dk, "dk"), (dv, "dv")):
+        _require(t, n, torch.bfloat16, 4)
+        if t.shape != q.shape:
+            raise ValueError(f"{n} must match q")
+    st = lib.fa_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), dout.data_ptr(),
+                    dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, N, d, 1 if causal else 0, float(scale),
+                    _stream_handle(stream))
+    _check(st, "fa_bwd")
+    return dq, dk, dv
+
+
+def fa_bwd_plan(N: int, d: int, block: int = 128, causal: bool = False) -> int:
+    """Number of fp32 additions into dQ that fa_bwd makes (host only)."""
+    lib = load_library()
+    adds = ctypes.c_longlong(0)
+    _check(lib.fa_bwd_plan(N, d, block, 1 if causal else 0, ctypes.byref(adds)), "fa_bwd_plan")
+    return adds.value
 
 
 def fa_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, seqlens: torch.Tensor,

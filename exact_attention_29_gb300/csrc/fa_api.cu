@@ -204,6 +204,57 @@ fa_status fa_decode(const void* q, const void* k_cache, const void* v_cache, con
   return st;
 }
 
+fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
+                 void* dq, void* dk, void* dv, int B, int H, int N, int d, int causal, float scale, fa_stream_t stream) {
+  if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv) return FA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned4(lse) || !aligned16(dout) ||
+      !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
+    return FA_ERR_INVALID_ARG;
+  if (B < 1 || H < 1 || N < 1 || d < 1) return FA_ERR_INVALID_ARG;
+  if (!(scale > 0.f) || !std::isfinite(scale)) return FA_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  const long long bh = static_cast<long long>(B) * H;
+  if (bh > 0x7fffffffLL || (static_cast<long long>(N) + 127) / 128 > 65535) return FA_ERR_INVALID_ARG;
+  int dev = -1;
+  fa_status st = current_device(&dev);
+  if (st != FA_OK) return st;
+  unsigned int* err = device_error_word();
+  if (!err) return FA_ERR_CUDA;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const size_t rows = static_cast<size_t>(bh) * N;
+  void* ws = nullptr;
+  cudaError_t e = cudaMallocAsync(&ws, rows * (d + 1) * sizeof(float), s);
+  if (e != cudaSuccess) {
+    set_error_text("cudaMallocAsync(backward workspace)", e);
+    return FA_ERR_CUDA;
+  }
+  float* dq_acc = static_cast<float*>(ws);
+  float* delta = dq_acc + rows * d;
+  st = launch_bwd(q, k, v, o, lse, dout, dq, dk, dv, B, H, N, d, causal, scale, dq_acc, delta, s, err);
+  e = cudaFreeAsync(ws, s);
+  if (st == FA_OK && e != cudaSuccess) {
+    set_error_text("cudaFreeAsync(backward workspace)", e);
+    st = FA_ERR_CUDA;
+  }
+  return st;
+}
+
+fa_status fa_bwd_plan(int N, int d, int block, int causal, long long* dq_atomic_adds) {
+  if (N < 1 || d < 1 || block < 1 || !dq_atomic_adds) return FA_ERR_INVALID_ARG;
+  const long long t = (static_cast<long long>(N) + block - 1) / block;
+  long long adds = 0;
+  for (long long j = 0; j < t; ++j) {
+    // Q tiles that see K/V tile j, each adding its rows (clipped to N) to dQ
+    for (long long i = (causal ? j : 0); i < t; ++i) {
+      const long long rows = (i * block + block <= N) ? block : (N - i * block);
+      adds += rows * d;
+    }
+  }
+  *dq_atomic_adds = adds;
+  return FA_OK;
+}
+
 fa_status fa_check_device_error(fa_stream_t stream, int* site) {
   if (site) *site = 0;
   cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));

@@ -30,6 +30,11 @@ fa_status launch_decode(const void* q, const void* k_cache, const void* v_cache,
                         float* lse, int B, int H, int L, int d, int num_splits, float* ws_o, float* ws_lse,
                         cudaStream_t stream);
 
+// dq_acc: fp32 [B*H*N*d] scratch (zeroed by the call), delta: fp32 [B*H*N] scratch.
+fa_status launch_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
+                     void* dq, void* dk, void* dv, int B, int H, int N, int d, int causal, float scale, float* dq_acc,
+                     float* delta, cudaStream_t stream, unsigned int* err);
+
 fa_status launch_selftest_mma(int mode, const void* a, const void* b, float* d, int n, int k, cudaStream_t stream,
                               unsigned int* err);
 fa_status launch_selftest_wait(unsigned int timeout_us, cudaStream_t stream, unsigned int* err);

@@ -45,4 +45,20 @@ __device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem, uint3
   }
 }
 
+// D(tmem, 128 x N fp32) = A(smem, 128 x 128, MN-major) * B(smem, 128 x N, MN-major).
+// A is stored transposed (rows are the contraction index, the 128 M values of a
+// row contiguous in two 64-element chunks) and B likewise (rows are the
+// contraction index, N contiguous): the dQ = dS K product of the backward pass,
+// with dS held as dS^T.
+template <int N>
+__device__ __forceinline__ void issue_mn_mn(uint32_t d_tmem, uint32_t a_smem, uint32_t b_smem) {
+  constexpr uint32_t idesc = idesc_bf16_f32(kBM, N, true, true);
+#pragma unroll
+  for (int kk = 0; kk < 128 / 16; ++kk) {
+    // 16 contraction rows = two 8-row groups of 1024 bytes in both operands
+    umma_ss(d_tmem, smem_desc_sw128(a_smem + static_cast<uint32_t>(kk * 2048), kChunkBytes, 1024),
+            smem_desc_sw128(b_smem + static_cast<uint32_t>(kk * 2048), kChunkBytes, 1024), idesc, kk > 0 ? 1u : 0u);
+  }
+}
+
 }  // namespace fa

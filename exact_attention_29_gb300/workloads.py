@@ -107,6 +107,13 @@ def prefill_inputs(B: int, H: int, N: int, d: int, seed: int = 0, device="cpu"):
     return q, k, v
 
 
+def backward_inputs(B: int, H: int, N: int, d: int, seed: int = 0, device="cpu"):
+    """The upstream gradient dO, bf16 [B, H, N, d], from its own seeded stream
+    (independent of the Q, K, V drawn by prefill_inputs with the same seed)."""
+    g = _generator(seed + 7919, B * H * N * d, device)
+    return _randn_bf16((B, H, N, d), g, device)
+
+
 def decode_inputs(B: int, H: int, L: int, d: int, seed: int = 0, ragged: bool = False,
                   device="cpu", lo: int = 1024):
     """q [B,H,d], K/V caches [B,H,L,d] (bf16) and seqlens [B] (int32)."""

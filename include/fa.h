@@ -69,6 +69,39 @@ fa_status fa_fwd(const void *q, const void *k, const void *v, void *o, float *ls
                  int causal, float scale, fa_stream_t stream);
 
 /*
+ * Backward pass (gradients of fa_fwd) with recomputation.
+ *
+ * Defines: CMU 15-779 Lecture 5 notes §7.1-7.4 and "FlashAttention 完全拆解
+ *   （一）", backward section: with S' = scale Q K^T (+ causal mask),
+ *   P = softmax(S'), O = P V and the upstream gradient dO,
+ *     dV = P^T dO, dP = dO V^T, dS = P * (dP - D) with D_i = dO_i . O_i,
+ *     dQ = scale dS K, dK = scale dS^T Q.
+ *   P is recomputed from the forward's per-row log-sum-exp, block by block;
+ *   K/V blocks form the outer loop (dK, dV accumulate on chip) and every block
+ *   adds its share of dQ with atomic additions in fp32.
+ *
+ *   q, k, v, o, dout  bf16 [B][H][N][d] (o and lse are fa_fwd's outputs for
+ *                     the same q, k, v, causal, scale). 16-byte aligned.
+ *   lse      fp32 [B][H][N], natural log.
+ *   dq, dk, dv  bf16 [B][H][N][d] outputs.
+ *   B, H, N, d, causal, scale: as fa_fwd.
+ * Workspace: B*H*N*(d+1)*4 bytes of stream-ordered device memory
+ *   (cudaMallocAsync on `stream`, freed on it): the fp32 dQ accumulator and D.
+ * Errors: as fa_fwd.
+ */
+fa_status fa_bwd(const void *q, const void *k, const void *v, const void *o, const float *lse, const void *dout,
+                 void *dq, void *dk, void *dv, int B, int H, int N, int d, int causal, float scale,
+                 fa_stream_t stream);
+
+/*
+ * Atomic work plan of fa_bwd (host only): with square tiles of `block` rows,
+ * the number of fp32 additions into dQ, i.e. for every K/V tile, the rows of
+ * every Q tile that sees it times d. Without the mask this is
+ * ceil(N/block) * N * d (CMU 15-779 Lecture 5 notes §7.4). fa_bwd uses 128.
+ */
+fa_status fa_bwd_plan(int N, int d, int block, int causal, long long *dq_atomic_adds);
+
+/*
  * Decode attention (Flash-Decoding).
  *
  * Defines: CMU 15-779 Lecture 5 notes §8.4 (split K/V along the sequence into

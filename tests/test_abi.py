@@ -154,3 +154,27 @@ def test_package_import_does_not_need_the_library(monkeypatch):
     with pytest.raises(RuntimeError, match="missing"):
         L.load_library()
     importlib.reload(L)
+
+
+def test_bwd_atomic_plan_matches_the_page(lib):
+    """Lecture 5 notes §7.4: ceil(N/B_c) * N * d dQ additions, 67,200 at N = 300, d = 32, B_c = 48."""
+    import exact_attention_29_gb300 as fa
+
+    g = json.load(open(os.path.join(GOLDEN, "bwd_atomics.json")))
+    assert fa.fa_bwd_plan(g["N"], g["d"], g["B_c"], causal=False) == g["dq_atomic_adds"]
+    # under the causal mask K/V tile j is seen by Q tiles j.. only
+    assert fa.fa_bwd_plan(256, 8, 128, causal=True) == (256 + 128) * 8
+
+
+def test_bwd_rejects_bad_arguments(lib):
+    import exact_attention_29_gb300 as fa
+
+    def bwd(q=16, d=128, N=128, scale=0.1, causal=0):
+        return lib.fa_bwd(q, 16, 16, 16, 16, 16, 16, 16, 16, 1, 1, N, d, causal, scale, None)
+
+    assert bwd(q=None) == fa.FA_ERR_INVALID_ARG
+    assert bwd(q=8) == fa.FA_ERR_INVALID_ARG
+    assert bwd(N=0) == fa.FA_ERR_INVALID_ARG
+    assert bwd(scale=-1.0) == fa.FA_ERR_INVALID_ARG
+    assert bwd(causal=3) == fa.FA_ERR_INVALID_ARG
+    assert bwd(d=96) == fa.FA_ERR_UNSUPPORTED
