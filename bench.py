@@ -302,6 +302,29 @@ def run_gpu(args, world, rank, local):
     value = world * fwd_flops * args.steps / (fwd_ms * 1e-3) / 1e12
     dec_gbs = world * kv_bytes * args.steps / (dec_ms * 1e-3) / 1e9
 
+    # backward (gradients of the same prefill), timed on its own after the step loop
+    bwd_steps = max(1, min(args.steps, 50))
+    gdo = wl.backward_inputs(pc.B, pc.H, pc.N, pc.d, seed=rank, device=dev)
+    gq, gk, gv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
+
+    def bwd_step():
+        fa.fa_bwd(q, k, v, o, lse, gdo, causal=pc.causal, dq=gq, dk=gk, dv=gv, stream=stream)
+
+    for _ in range(3):
+        bwd_step()
+    torch.cuda.synchronize(dev)
+    b0 = torch.cuda.Event(enable_timing=True)
+    b1 = torch.cuda.Event(enable_timing=True)
+    b0.record(stream)
+    for _ in range(bwd_steps):
+        bwd_step()
+    b1.record(stream)
+    torch.cuda.synchronize(dev)
+    fa.fa_check_device_error(stream)
+    bwd_ms = reduce_max([b0.elapsed_time(b1)], world)[0]
+    bwd_flops = perfmodel.bwd_flops(pc.B, pc.H, pc.N, pc.d, pc.causal)
+    bwd_value = world * bwd_flops * bwd_steps / (bwd_ms * 1e-3) / 1e12
+
     # end to end through the public API with pinned host buffers: H2D of q/k/v,
     # the C-ABI call, D2H of o and lse, all inside the timed region
     hq, hk, hv = (t.cpu().pin_memory() for t in (q, k, v))
@@ -363,6 +386,11 @@ def run_gpu(args, world, rank, local):
         "decode": {"value": dec_gbs, "unit": "GB/s (KV read)", "frac_of_hbm": dec_gbs / peaks["hbm_gbs"],
                    "ms_per_step": dec_avg_ms},
         "prefill_ms_per_step": fwd_avg_ms,
+        "backward": {"value": bwd_value, "unit": "TFLOP/s (10 N^2 d per head, halved causal)",
+                     "ms_per_call": bwd_ms / bwd_steps, "steps": bwd_steps,
+                     "frac_of_bf16_peak": bwd_value / world / peaks["bf16_tflops"],
+                     "what": "fa_bwd on the prefill workload (dQ zeroing, D, main kernel, dQ conversion), "
+                             "timed after the step loop"},
         "prefill_frac_of_bf16_peak": value / world / tflops_peak,
         "roofline": dominant,
         "rooflines": {"fwd": fwd_roof, "decode": dec_roof},

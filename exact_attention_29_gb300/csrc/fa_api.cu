@@ -101,8 +101,12 @@ unsigned int* device_error_word() {
   return g_err_ptr[dev];
 }
 
-bool encode_bf16_map(CUtensorMap* map, const void* base, uint64_t d, uint64_t rows, uint64_t outer,
-                     uint32_t box_rows) {
+namespace {
+
+// A 3-D map over [outer][rows][d] with 128-byte swizzle and a box of
+// box_inner x box_rows x 1 elements (box_inner x elem_bytes = 128 bytes).
+bool encode_3d(CUtensorMap* map, CUtensorMapDataType dtype, uint64_t elem_bytes, uint32_t box_inner, const void* base,
+               uint64_t d, uint64_t rows, uint64_t outer, uint32_t box_rows) {
   {
     std::lock_guard<std::mutex> lock(g_mutex);
     if (g_encode == nullptr) {
@@ -118,11 +122,11 @@ bool encode_bf16_map(CUtensorMap* map, const void* base, uint64_t d, uint64_t ro
     }
   }
   const cuuint64_t dims[3] = {d, rows, outer};
-  const cuuint64_t strides[2] = {d * 2, rows * d * 2};
-  const cuuint32_t box[3] = {64, box_rows, 1};
+  const cuuint64_t strides[2] = {d * elem_bytes, rows * d * elem_bytes};
+  const cuuint32_t box[3] = {box_inner, box_rows, 1};
   const cuuint32_t estr[3] = {1, 1, 1};
-  const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
-                              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+  const CUresult r = g_encode(map, dtype, 3, const_cast<void*>(base), dims, strides, box, estr,
+                              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) {
     char buf[64];
@@ -131,6 +135,18 @@ bool encode_bf16_map(CUtensorMap* map, const void* base, uint64_t d, uint64_t ro
     return false;
   }
   return true;
+}
+
+}  // namespace
+
+bool encode_bf16_map(CUtensorMap* map, const void* base, uint64_t d, uint64_t rows, uint64_t outer,
+                     uint32_t box_rows) {
+  return encode_3d(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 64, base, d, rows, outer, box_rows);
+}
+
+bool encode_f32_map(CUtensorMap* map, const void* base, uint64_t d, uint64_t rows, uint64_t outer,
+                    uint32_t box_rows) {
+  return encode_3d(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, 32, base, d, rows, outer, box_rows);
 }
 
 }  // namespace fa

@@ -9,15 +9,29 @@
 // chip and are written once; every K/V block adds its share of dQ into an fp32
 // buffer with atomic adds (§7.4).
 //
-// Mapping onto one CTA (one K/V tile of 128 keys of one head, 128 threads):
-//   TMEM columns: [0,128) S^T = K Q^T, then P^T (bf16 pairs, first 64
-//   columns), then the dQ share dS K; [128,256) dP^T = V dO^T, then dS^T;
-//   [256, 256+D) dV; [384, 384+D) dK.
-//   Thread r owns key row r of S^T, dP^T, dV and dK, and query row r of the
-//   dQ share. Thread 0 issues every TMA copy and tensor-core product; the
-//   phases of a Q tile are separated by mbarrier waits and block barriers.
-//   dS^T also goes to shared memory in the 128-byte-swizzled MN-major layout
-//   so that dS (queries x keys) can be the A operand of dQ = dS K.
+// One CTA owns one K/V tile (128 keys) of one head and walks the Q tiles that
+// see it. Everything is computed transposed, keys on the 128 TMEM lanes:
+//   TMEM columns [0,128)    S^T = K Q^T, then P^T as bf16 pairs
+//            [128,256)  dP^T = V dO^T, then dS^T as bf16 pairs, then the
+//                       dQ share dS K (lanes = queries, D columns)
+//            [256,256+D) dV,  [384,384+D) dK  (fp32 accumulators)
+// Warp roles (14 warps):
+//   warp 12     TMA: K and V once; Q (two buffers) and dO (one buffer) per Q
+//               tile, plus that tile's row statistics (L log2 e, D) into shared
+//               memory.
+//   warp 13     one thread issues every tensor-core product, in the order
+//                 dV_i, S_{i+1}, dK_i, dQ_i, dP_{i+1}
+//               so that S of the next tile runs while P/dS warps finish dS_i,
+//               and dP_{i+1} waits only for the read-out of dQ_i.
+//   warps 4-11  P and dS: warp w takes key rows 32(w%4).. and query columns
+//               64((w-4)/4)..; P = exp2(S log2e scale - L log2e) (kept in fp32
+//               registers), bf16 P^T to TMEM (for dV), then dS = P (dP - D) to
+//               TMEM (for dK) and, transposed, to shared memory (for dQ = dS K,
+//               whose A operand must be query-major).
+//   warps 0-3   read the dQ share out of TMEM, stage it in shared memory and
+//               add scale * dQ to the fp32 accumulator with bulk tensor
+//               reductions (the atomic additions of §7.4, done by the TMA unit
+//               on whole 128-byte rows).
 // Every wait is bounded (fa_common.cuh).
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -31,7 +45,11 @@
 namespace fa {
 namespace {
 
-constexpr int kBwdThreads = 128;
+constexpr int kLoadWarp = 12;
+constexpr int kMmaWarp = 13;
+// 14 warps: each SM sub-partition holds at most four of them, so a thread can
+// have 16,384 / (4 x 32) = 128 registers.
+constexpr int kBwdThreads = 14 * 32;
 constexpr uint32_t kFull = 0xffffffffu;
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -42,13 +60,33 @@ struct BwdCfg {
   static constexpr int kDsBytes = 128 * 128 * 2;  // dS^T, 128 keys x 128 queries
   static constexpr int kKOff = 0;
   static constexpr int kVOff = kTileBytes;
-  static constexpr int kQOff = 2 * kTileBytes;
-  static constexpr int kDoOff = 3 * kTileBytes;
-  static constexpr int kDsOff = 4 * kTileBytes;
-  static constexpr int kVecOff = kDsOff + kDsBytes;  // lse2[128], delta[128]
-  static constexpr int kBarOff = kVecOff + 2 * 128 * 4;
-  static constexpr int kSmemBytes = kBarOff + 8 * 8 + 1024;
+  static constexpr int kQOff = 2 * kTileBytes;  // two buffers
+  static constexpr int kDoOff = 4 * kTileBytes;
+  static constexpr int kDsOff = 5 * kTileBytes;
+  static constexpr int kBoxBytes = 128 * 32 * 4;      // one dQ staging box: 128 rows x 32 fp32
+  static constexpr int kStageOff = kDsOff + kDsBytes;  // third staging box (d = 128)
+  static constexpr int kVecOff = kStageOff + kBoxBytes;  // [2][128] L log2 e, then [2][128] D
+  static constexpr int kBarOff = kVecOff + 4 * 128 * 4;
+  static constexpr int kSmemBytes = kBarOff + 256 + 1024;
   static constexpr uint32_t kColS = 0, kColDp = 128, kColDv = 256, kColDk = 384;
+};
+
+// barrier slots
+enum BwdBar : int {
+  kBarKv = 0,
+  kBarQFull = 1,   // +buffer
+  kBarQEmpty = 3,  // +buffer
+  kBarDoFull = 5,
+  kBarDoEmpty = 6,
+  kBarVec = 7,  // +buffer
+  kBarS = 9,
+  kBarDp = 10,
+  kBarP = 11,
+  kBarDs = 12,
+  kBarDq = 13,
+  kBarDqEmpty = 14,
+  kBarAcc = 15,
+  kNumBars = 16,
 };
 
 struct BwdParams {
@@ -100,16 +138,11 @@ __global__ void __launch_bounds__(256) bwd_dq_convert_kernel(const float* __rest
   reinterpret_cast<uint2*>(dq)[i] = w;
 }
 
-__device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float c, float d) {
-  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
-               : "memory");
-}
-
 template <int D>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-               const BwdParams p) {
+               const __grid_constant__ CUtensorMap tm_dq, const BwdParams p) {
   using C = BwdCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -118,29 +151,41 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   uint8_t* sq = base + C::kQOff;
   uint8_t* sdo = base + C::kDoOff;
   uint8_t* sds = base + C::kDsOff;
-  float* lse2 = reinterpret_cast<float*>(base + C::kVecOff);
-  float* dlt = lse2 + 128;
+  uint8_t* sstage = base + C::kStageOff;
+  float* vec_l = reinterpret_cast<float*>(base + C::kVecOff);  // [2][128]
+  float* vec_d = vec_l + 256;                                  // [2][128]
   uint64_t* bars = reinterpret_cast<uint64_t*>(base + C::kBarOff);
-  uint64_t* kv_bar = &bars[0];
-  uint64_t* qdo_bar = &bars[1];
-  uint64_t* mma_bar = &bars[2];
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(&bars[4]);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(&bars[5]);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(&bars[kNumBars]);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(&bars[kNumBars + 1]);
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
-  // grid (heads, K/V tiles): blocks launch in order of K/V tile, and under the
+  // grid (heads, K/V tiles): blocks start in order of K/V tile, and under the
   // causal mask tile 0 (seen by every Q tile) is the heaviest
   const int bh = blockIdx.x;
   const int j = blockIdx.y;
   const int kv0 = j * 128;
   const int num_q_tiles = (p.N + 127) / 128;
-  const int i_first = p.causal ? j : 0;  // Q tiles whose rows see some key of this tile
+  const int i_first = p.causal ? j : 0;  // first Q tile whose rows see a key of this tile
+  const int n_it = num_q_tiles - i_first;  // >= 1 since j < num_q_tiles
+  const size_t head_rows = static_cast<size_t>(bh) * p.N;
 
   if (tid == 0) {
-    mbar_init(kv_bar, 1);
-    mbar_init(qdo_bar, 1);
-    mbar_init(mma_bar, 1);
+    mbar_init(&bars[kBarKv], 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&bars[kBarQFull + b], 1);
+      mbar_init(&bars[kBarQEmpty + b], 1);
+      mbar_init(&bars[kBarVec + b], 32);
+    }
+    mbar_init(&bars[kBarDoFull], 1);
+    mbar_init(&bars[kBarDoEmpty], 1);
+    mbar_init(&bars[kBarS], 1);
+    mbar_init(&bars[kBarDp], 1);
+    mbar_init(&bars[kBarP], 8);
+    mbar_init(&bars[kBarDs], 8);
+    mbar_init(&bars[kBarDq], 1);
+    mbar_init(&bars[kBarDqEmpty], 4);
+    mbar_init(&bars[kBarAcc], 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -152,182 +197,304 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
-  const int row = warp * 32 + lane;  // key row (S^T, dP^T, dV, dK) and query row (dQ share)
 
-  if (tid == 0) {
-    tma_prefetch_desc(&tm_q);
-    tma_prefetch_desc(&tm_do);
-    mbar_arrive_expect_tx(kv_bar, 2 * C::kTileBytes);
-#pragma unroll
-    for (int c = 0; c < C::kChunks; ++c) {
-      tma_load_3d(sk + c * kChunkBytes, &tm_k, kv_bar, c * 64, kv0, bh);
-      tma_load_3d(sv + c * kChunkBytes, &tm_v, kv_bar, c * 64, kv0, bh);
-    }
-  }
-  bool ok = bounded_wait(kv_bar, 0, abort_flag, p.err, kSiteKvFull);
-  uint32_t mma_phase = 0;
-  int qdo_issued = 0;  // Q/dO tile pairs requested by thread 0
-  const size_t head_rows = static_cast<size_t>(bh) * p.N;
-
-  for (int i = i_first; i < num_q_tiles && ok; ++i) {
-    const int q0 = i * 128;
-    const int it = i - i_first;
-    // (a) Q_i and dO_i by TMA; the row statistics by plain loads
-    if (tid == 0) {
-      mbar_arrive_expect_tx(qdo_bar, 2 * C::kTileBytes);
+  if (warp == kLoadWarp) {
+    // ---------------------------------------------------------------- loads
+    int q_cnt0 = 0, q_cnt1 = 0, do_cnt = 0;
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_do);
+      mbar_arrive_expect_tx(&bars[kBarKv], 2 * C::kTileBytes);
 #pragma unroll
       for (int c = 0; c < C::kChunks; ++c) {
-        tma_load_3d(sq + c * kChunkBytes, &tm_q, qdo_bar, c * 64, q0, bh);
-        tma_load_3d(sdo + c * kChunkBytes, &tm_do, qdo_bar, c * 64, q0, bh);
+        tma_load_3d(sk + c * kChunkBytes, &tm_k, &bars[kBarKv], c * 64, kv0, bh);
+        tma_load_3d(sv + c * kChunkBytes, &tm_v, &bars[kBarKv], c * 64, kv0, bh);
       }
-      ++qdo_issued;
     }
-    {
-      const int qr = q0 + tid;
-      // rows beyond N: L = +inf makes P = 0 there, and D = 0
-      lse2[tid] = (qr < p.N) ? p.lse[head_rows + qr] * kLog2e : INFINITY;
-      dlt[tid] = (qr < p.N) ? p.delta[head_rows + qr] : 0.f;
+    bool ok = true;
+    for (int it = 0; it < n_it && ok; ++it) {
+      const int b = it & 1;
+      const int q0 = (i_first + it) * 128;
+      if (it >= 2) ok = bounded_wait(&bars[kBarQEmpty + b], ((it - 2) >> 1) & 1, abort_flag, p.err, kSiteQEmpty);
+      if (!__all_sync(kFull, ok)) break;
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&bars[kBarQFull + b], C::kTileBytes);
+#pragma unroll
+        for (int c = 0; c < C::kChunks; ++c)
+          tma_load_3d(sq + b * C::kTileBytes + c * kChunkBytes, &tm_q, &bars[kBarQFull + b], c * 64, q0, bh);
+        if (b == 0)
+          ++q_cnt0;
+        else
+          ++q_cnt1;
+      }
+      // row statistics of this Q tile; rows beyond N get L = +inf (P = 0) and D = 0
+#pragma unroll
+      for (int r = lane; r < 128; r += 32) {
+        const int qr = q0 + r;
+        vec_l[b * 128 + r] = (qr < p.N) ? p.lse[head_rows + qr] * kLog2e : INFINITY;
+        vec_d[b * 128 + r] = (qr < p.N) ? p.delta[head_rows + qr] : 0.f;
+      }
+      mbar_arrive(&bars[kBarVec + b]);
+      if (it >= 1) ok = bounded_wait(&bars[kBarDoEmpty], (it - 1) & 1, abort_flag, p.err, kSiteOEmpty);
+      if (!__all_sync(kFull, ok)) break;
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&bars[kBarDoFull], C::kTileBytes);
+#pragma unroll
+        for (int c = 0; c < C::kChunks; ++c)
+          tma_load_3d(sdo + c * kChunkBytes, &tm_do, &bars[kBarDoFull], c * 64, q0, bh);
+        ++do_cnt;
+      }
     }
-    __syncthreads();
-    ok = bounded_wait(qdo_bar, it & 1, abort_flag, p.err, kSiteQFull);
-    ok = __all_sync(kFull, ok) && ok;
-    if (!__syncthreads_and(ok)) break;
-
-    // (b) S^T = K Q^T and dP^T = V dO^T
-    if (tid == 0) {
-      tc_fence_after();
-      issue_qk<D>(tmem + C::kColS, smem_u32(sk), smem_u32(sq));
-      issue_qk<D>(tmem + C::kColDp, smem_u32(sv), smem_u32(sdo));
-      umma_commit(mma_bar);
+    // every copy issued must land before the CTA exits
+    if (lane == 0) {
+      bounded_wait(&bars[kBarKv], 0, nullptr, p.err, kSiteDrain);
+      if (q_cnt0 > 0) bounded_wait(&bars[kBarQFull], (q_cnt0 - 1) & 1, nullptr, p.err, kSiteDrain);
+      if (q_cnt1 > 0) bounded_wait(&bars[kBarQFull + 1], (q_cnt1 - 1) & 1, nullptr, p.err, kSiteDrain);
+      if (do_cnt > 0) bounded_wait(&bars[kBarDoFull], (do_cnt - 1) & 1, nullptr, p.err, kSiteDrain);
     }
-    __syncwarp();
-    ok = bounded_wait(mma_bar, mma_phase & 1, abort_flag, p.err, kSiteSFull);
-    ++mma_phase;
-    ok = __all_sync(kFull, ok);
-    if (!__syncthreads_and(ok)) break;
-    tc_fence_after();
-
-    // (c) P^T and dS^T for key row `row`, 32 queries at a time
+  } else if (warp == kMmaWarp) {
+    // ---------------------------------------------------------------- products
+    if (lane == 0) {
+      const uint32_t s_tm = tmem + C::kColS, dp_tm = tmem + C::kColDp;
+      bool ok = bounded_wait(&bars[kBarKv], 0, abort_flag, p.err, kSiteKvFull) &&
+                bounded_wait(&bars[kBarQFull], 0, abort_flag, p.err, kSiteQFull);
+      if (ok) {
+        tc_fence_after();
+        issue_qk<D>(s_tm, smem_u32(sk), smem_u32(sq));
+        umma_commit(&bars[kBarS]);
+        ok = bounded_wait(&bars[kBarDoFull], 0, abort_flag, p.err, kSiteQFull);
+      }
+      if (ok) {
+        tc_fence_after();
+        issue_qk<D>(dp_tm, smem_u32(sv), smem_u32(sdo));
+        umma_commit(&bars[kBarDp]);
+      }
+      for (int it = 0; it < n_it && ok; ++it) {
+        const int b = it & 1;
+        const bool more = it + 1 < n_it;
+        // dV += P^T dO as soon as P^T is in TMEM
+        if (!(ok = bounded_wait(&bars[kBarP], it & 1, abort_flag, p.err, kSitePFull))) break;
+        tc_fence_after();
+        issue_pv<D>(tmem + C::kColDv, s_tm, smem_u32(sdo), it > 0, 32);
+        umma_commit(&bars[kBarDoEmpty]);
+        // S of the next Q tile overwrites P^T behind the dV product
+        if (more) {
+          if (!(ok = bounded_wait(&bars[kBarQFull + (b ^ 1)], ((it + 1) >> 1) & 1, abort_flag, p.err, kSiteQFull)))
+            break;
+          tc_fence_after();
+          issue_qk<D>(s_tm, smem_u32(sk), smem_u32(sq + (b ^ 1) * C::kTileBytes));
+          umma_commit(&bars[kBarS]);
+        }
+        // dK += dS^T Q, then the dQ share dS K into the dP columns
+        if (!(ok = bounded_wait(&bars[kBarDs], it & 1, abort_flag, p.err, kSitePFull))) break;
+        tc_fence_after();
+        issue_pv<D>(tmem + C::kColDk, dp_tm, smem_u32(sq + b * C::kTileBytes), it > 0, 32);
+        umma_commit(&bars[kBarQEmpty + b]);
+        issue_mn_mn<D>(dp_tm, smem_u32(sds), smem_u32(sk));
+        umma_commit(&bars[kBarDq]);
+        // dP of the next tile once the dQ share has been read out
+        if (more) {
+          if (!(ok = bounded_wait(&bars[kBarDqEmpty], it & 1, abort_flag, p.err, kSiteOEmpty))) break;
+          if (!(ok = bounded_wait(&bars[kBarDoFull], (it + 1) & 1, abort_flag, p.err, kSiteQFull))) break;
+          tc_fence_after();
+          issue_qk<D>(dp_tm, smem_u32(sv), smem_u32(sdo));
+          umma_commit(&bars[kBarDp]);
+        }
+      }
+      // completes once every product above has; the epilogue reads dK and dV after it
+      umma_commit(&bars[kBarAcc]);
+      bounded_wait(&bars[kBarAcc], 0, nullptr, p.err, kSiteDrain);
+    }
+  } else if (warp >= 4) {
+    // ---------------------------------------------------------------- P and dS
+    const int quad = warp & 3, half = (warp - 4) >> 2;
+    const int row = quad * 32 + lane;  // key row within the tile
+    const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
     const int key = kv0 + row;
     const bool key_ok = key < p.N;
-#pragma unroll 1
-    for (int ch = 0; ch < 4; ++ch) {
-      uint32_t s[32], dp[32];
-      tmem_ld_x32(tmem + lane_base + C::kColS + 32 * ch, s);
-      tmem_ld_x32(tmem + lane_base + C::kColDp + 32 * ch, dp);
-      uint32_t pw[16], dw[16];
-#pragma unroll
-      for (int e = 0; e < 16; ++e) {
-        float pv[2], dv[2];
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int c = 32 * ch + 2 * e + h;
-          const int q = q0 + c;
-          float pr = ex2_approx(fmaf(__uint_as_float(s[2 * e + h]), p.scale_log2, -lse2[c]));
-          if (!key_ok || (p.causal && key > q)) pr = 0.f;
-          pv[h] = pr;
-          dv[h] = pr * (__uint_as_float(dp[2 * e + h]) - dlt[c]);
-        }
-        pw[e] = pack_bf16x2(pv[0], pv[1]);
-        dw[e] = pack_bf16x2(dv[0], dv[1]);
+    const uint64_t sc2 = f2_pack(p.scale_log2, p.scale_log2);
+    const uint32_t s_tm = tmem + lane_base + C::kColS + 64 * half;
+    const uint32_t dp_tm = tmem + lane_base + C::kColDp + 64 * half;
+    uint8_t* ds_row = sds + half * kChunkBytes + row * 128;
+    bool ok = true;
+    for (int it = 0; it < n_it; ++it) {
+      const int b = it & 1;
+      const int i = i_first + it;
+      ok = bounded_wait(&bars[kBarS], it & 1, abort_flag, p.err, kSiteSFull) &&
+           bounded_wait(&bars[kBarVec + b], (it >> 1) & 1, abort_flag, p.err, kSiteQFull);
+      if (!__all_sync(kFull, ok)) {
+        ok = false;
+        break;
       }
-      // P^T and dS^T pairs overwrite score columns this thread has already read
-      tmem_st_x16(tmem + lane_base + C::kColS + 16 * ch, pw);
-      tmem_st_x16(tmem + lane_base + C::kColDp + 16 * ch, dw);
-      // dS^T row `row`, queries [32ch, 32ch + 32): four 16-byte units of the
-      // 128-byte row of chunk (ch / 2), swizzled by the row index
-      uint8_t* rowp = sds + (ch >> 1) * kChunkBytes + row * 128;
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int unit = (ch & 1) * 4 + u;
-        *reinterpret_cast<uint4*>(rowp + ((unit ^ (row & 7)) << 4)) =
-            make_uint4(dw[4 * u], dw[4 * u + 1], dw[4 * u + 2], dw[4 * u + 3]);
-      }
-    }
-    tmem_st_wait();
-    fence_proxy_async_smem();
-    tc_fence_before();
-    __syncthreads();
-
-    // (d) dV += P^T dO, dK += dS^T Q, dQ share = dS K
-    if (tid == 0) {
       tc_fence_after();
-      issue_pv<D>(tmem + C::kColDv, tmem + C::kColS, smem_u32(sdo), it > 0);
-      issue_pv<D>(tmem + C::kColDk, tmem + C::kColDp, smem_u32(sq), it > 0);
-      issue_mn_mn<D>(tmem + C::kColS, smem_u32(sds), smem_u32(sk));
-      umma_commit(mma_bar);
-    }
-    __syncwarp();
-    ok = bounded_wait(mma_bar, mma_phase & 1, abort_flag, p.err, kSitePFull);
-    ++mma_phase;
-    ok = __all_sync(kFull, ok);
-    if (!__syncthreads_and(ok)) break;
-    tc_fence_after();
+      // P^T for this row and 64 queries, fp32 in registers
+      float pf[64];
+      const float4* l4 = reinterpret_cast<const float4*>(vec_l + b * 128 + 64 * half);
+#pragma unroll
+      for (int h2 = 0; h2 < 2; ++h2) {
+        uint32_t s[32];
+        tmem_ld_x32(s_tm + 32 * h2, s);
+#pragma unroll
+        for (int e4 = 0; e4 < 8; ++e4) {
+          const float4 l = l4[8 * h2 + e4];
+          const uint64_t a = f2_fma(f2_pack(__uint_as_float(s[4 * e4]), __uint_as_float(s[4 * e4 + 1])), sc2,
+                                    f2_pack(-l.x, -l.y));
+          const uint64_t c = f2_fma(f2_pack(__uint_as_float(s[4 * e4 + 2]), __uint_as_float(s[4 * e4 + 3])), sc2,
+                                    f2_pack(-l.z, -l.w));
+          float x0, x1, x2, x3;
+          f2_unpack(a, x0, x1);
+          f2_unpack(c, x2, x3);
+          const int e = 32 * h2 + 4 * e4;
+          pf[e] = ex2_approx(x0);
+          pf[e + 1] = ex2_approx(x1);
+          pf[e + 2] = ex2_approx(x2);
+          pf[e + 3] = ex2_approx(x3);
+        }
+      }
+      if (!key_ok) {
+#pragma unroll
+        for (int e = 0; e < 64; ++e) pf[e] = 0.f;
+      } else if (p.causal && i == j) {
+        // the diagonal tile: query 64 half + e sees this key only if it is not earlier
+#pragma unroll
+        for (int e = 0; e < 64; ++e)
+          if (row > 64 * half + e) pf[e] = 0.f;
+      }
+      {
+        uint32_t pw[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) pw[e] = pack_bf16x2(pf[2 * e], pf[2 * e + 1]);
+        tmem_st_x32(s_tm, pw);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[kBarP]);
 
-    // (e) add scale * (dS K) for query row `row` into dQ
-    {
-      const int q = q0 + row;
-      float* dst = p.dq_acc + (head_rows + (q < p.N ? q : 0)) * D;
+      // dS = P (dP - D)
+      ok = bounded_wait(&bars[kBarDp], it & 1, abort_flag, p.err, kSiteSFull);
+      if (!__all_sync(kFull, ok)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const float4* d4 = reinterpret_cast<const float4*>(vec_d + b * 128 + 64 * half);
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        uint32_t dp[32];
+        tmem_ld_x32(dp_tm + 32 * c, dp);
+        uint32_t dw[16];
+#pragma unroll
+        for (int e4 = 0; e4 < 8; ++e4) {
+          const float4 dl = d4[8 * c + e4];
+          const int e = 32 * c + 4 * e4;
+          const uint64_t a = f2_mul(f2_pack(pf[e], pf[e + 1]),
+                                    f2_add(f2_pack(__uint_as_float(dp[4 * e4]), __uint_as_float(dp[4 * e4 + 1])),
+                                           f2_pack(-dl.x, -dl.y)));
+          const uint64_t q = f2_mul(f2_pack(pf[e + 2], pf[e + 3]),
+                                    f2_add(f2_pack(__uint_as_float(dp[4 * e4 + 2]), __uint_as_float(dp[4 * e4 + 3])),
+                                           f2_pack(-dl.z, -dl.w)));
+          float x0, x1, x2, x3;
+          f2_unpack(a, x0, x1);
+          f2_unpack(q, x2, x3);
+          dw[2 * e4] = pack_bf16x2(x0, x1);
+          dw[2 * e4 + 1] = pack_bf16x2(x2, x3);
+        }
+        // dS^T pairs overwrite dP columns of this chunk that are already read
+        tmem_st_x16(dp_tm + 16 * c, dw);
+        // dS^T row `row`, queries 64 half + 32 c + [0, 32): 16-byte units
+        // 4c..4c+3 of the 128-byte row, swizzled by the row index
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          *reinterpret_cast<uint4*>(ds_row + (((4 * c + u) ^ (row & 7)) << 4)) =
+              make_uint4(dw[4 * u], dw[4 * u + 1], dw[4 * u + 2], dw[4 * u + 3]);
+      }
+      tmem_st_wait();
+      fence_proxy_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[kBarDs]);
+    }
+    // dK = scale * acc and dV = acc for this key row, columns of this half of d
+    if (ok) ok = bounded_wait(&bars[kBarAcc], 0, abort_flag, p.err, kSiteOFull);
+    if (__all_sync(kFull, ok)) {
+      tc_fence_after();
+      const size_t out = (head_rows + (key_ok ? key : 0)) * D;
 #pragma unroll 1
-      for (int c = 0; c < D; c += 32) {
+      for (int c = half * (D / 2); c < (half + 1) * (D / 2); c += 32) {
+        uint32_t a[32], v[32];
+        tmem_ld_x32(tmem + lane_base + C::kColDk + c, a);
+        tmem_ld_x32(tmem + lane_base + C::kColDv + c, v);
+        if (key_ok) {
+          uint32_t wk[16], wv[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            wk[e] = pack_bf16x2(__uint_as_float(a[2 * e]) * p.scale, __uint_as_float(a[2 * e + 1]) * p.scale);
+            wv[e] = pack_bf16x2(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1]));
+          }
+          uint4* pk = reinterpret_cast<uint4*>(p.dk + out + c);
+          uint4* pv = reinterpret_cast<uint4*>(p.dv + out + c);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            pk[e] = make_uint4(wk[4 * e], wk[4 * e + 1], wk[4 * e + 2], wk[4 * e + 3]);
+            pv[e] = make_uint4(wv[4 * e], wv[4 * e + 1], wv[4 * e + 2], wv[4 * e + 3]);
+          }
+        }
+      }
+    }
+  } else {
+    // ---------------------------------------------------------------- dQ read-out
+    // warp w owns query rows 32w.. of the dQ share. Each 32-column slice of
+    // dQ goes (scaled) into a shared-memory box in the tensor map's swizzled
+    // layout and one thread adds the box into the fp32 accumulator with a
+    // bulk tensor reduction; rows beyond N are clipped by the map.
+    // Boxes: slices 0 and 1 in the two halves of the dS^T buffer (free once
+    // the dQ product is complete and until the next dS is written, which
+    // waits for dq_empty), slice 2 in its own box, slice 3 in the first half
+    // again.
+    const int row = warp * 32 + lane;
+    const uint32_t dq_tm = tmem + (static_cast<uint32_t>(warp * 32) << 16) + C::kColDp;
+    const bool issuer = tid == 0;
+    if (issuer) tma_prefetch_desc(&tm_dq);
+    for (int it = 0; it < n_it; ++it) {
+      bool ok = bounded_wait(&bars[kBarDq], it & 1, abort_flag, p.err, kSitePFull);
+      // one decision for all four warps: they meet at named barriers below
+      if (!named_bar_and(1, 128, ok)) break;
+      tc_fence_after();
+      const int q0 = (i_first + it) * 128;
+#pragma unroll 1
+      for (int c = 0; c < D / 32; ++c) {
+        uint8_t* box = (c == 2) ? sstage : sds + (c == 1 ? C::kBoxBytes : 0);
+        if (c == 3) {
+          // slice 0's reduction must have finished reading the first half
+          if (issuer) bulk_wait_group_read<2>();
+          named_bar_sync(1, 128);
+        }
         uint32_t r[32];
-        tmem_ld_x32(tmem + lane_base + C::kColS + c, r);
-        if (q < p.N) {
+        tmem_ld_x32(dq_tm + 32 * c, r);
+        uint8_t* rowp = box + row * 128;
 #pragma unroll
-          for (int e = 0; e < 8; ++e)
-            red_add_v4(dst + c + 4 * e, __uint_as_float(r[4 * e]) * p.scale, __uint_as_float(r[4 * e + 1]) * p.scale,
-                       __uint_as_float(r[4 * e + 2]) * p.scale, __uint_as_float(r[4 * e + 3]) * p.scale);
+        for (int u = 0; u < 8; ++u)
+          *reinterpret_cast<float4*>(rowp + ((u ^ (row & 7)) << 4)) =
+              make_float4(__uint_as_float(r[4 * u]) * p.scale, __uint_as_float(r[4 * u + 1]) * p.scale,
+                          __uint_as_float(r[4 * u + 2]) * p.scale, __uint_as_float(r[4 * u + 3]) * p.scale);
+        fence_proxy_async_smem();
+        named_bar_sync(1, 128);
+        if (issuer) {
+          tma_reduce_add_3d(&tm_dq, box, 32 * c, q0, bh);
+          bulk_commit_group();
         }
       }
+      // the dS^T buffer is written again after the next dP: its reads must be done
+      if (issuer) bulk_wait_group_read<0>();
+      tc_fence_before();
+      named_bar_sync(1, 128);
+      if (lane == 0) mbar_arrive(&bars[kBarDqEmpty]);
     }
-    tc_fence_before();
-    __syncthreads();  // the next S^T overwrites these columns
+    // the additions must be complete before the CTA exits
+    if (issuer) bulk_wait_group<0>();
   }
 
-  // dK = scale * acc and dV = acc for key row `row`, written once
-  if (ok && i_first < num_q_tiles) {
-    tc_fence_after();
-    const int key = kv0 + row;
-    const size_t out = (head_rows + (key < p.N ? key : 0)) * D;
-#pragma unroll 1
-    for (int c = 0; c < D; c += 32) {
-      uint32_t a[32], b[32];
-      tmem_ld_x32(tmem + lane_base + C::kColDk + c, a);
-      tmem_ld_x32(tmem + lane_base + C::kColDv + c, b);
-      if (key < p.N) {
-        uint32_t wk[16], wv[16];
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          wk[e] = pack_bf16x2(__uint_as_float(a[2 * e]) * p.scale, __uint_as_float(a[2 * e + 1]) * p.scale);
-          wv[e] = pack_bf16x2(__uint_as_float(b[2 * e]), __uint_as_float(b[2 * e + 1]));
-        }
-        uint4* pk = reinterpret_cast<uint4*>(p.dk + out + c);
-        uint4* pv = reinterpret_cast<uint4*>(p.dv + out + c);
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          pk[e] = make_uint4(wk[4 * e], wk[4 * e + 1], wk[4 * e + 2], wk[4 * e + 3]);
-          pv[e] = make_uint4(wv[4 * e], wv[4 * e + 1], wv[4 * e + 2], wv[4 * e + 3]);
-        }
-      }
-    }
-  } else if (ok) {
-    // no Q tile sees this K/V tile (cannot happen for N >= 1, kept for safety): zero gradients
-    const int key = kv0 + row;
-    if (key < p.N) {
-      uint4* pk = reinterpret_cast<uint4*>(p.dk + (head_rows + key) * D);
-      uint4* pv = reinterpret_cast<uint4*>(p.dv + (head_rows + key) * D);
-      for (int e = 0; e < D / 8; ++e) pk[e] = pv[e] = make_uint4(0, 0, 0, 0);
-    }
-  }
-  // teardown: every copy must have landed and every product completed before
-  // the CTA exits and TMEM is freed
-  if (tid == 0) {
-    bounded_wait(kv_bar, 0, nullptr, p.err, kSiteDrain);
-    if (qdo_issued > 0) bounded_wait(qdo_bar, (qdo_issued - 1) & 1, nullptr, p.err, kSiteDrain);
-    umma_commit(mma_bar);
-    bounded_wait(mma_bar, mma_phase & 1, nullptr, p.err, kSiteDrain);
-  }
   tc_fence_before();
   __syncthreads();
   if (warp == 0) {
@@ -351,9 +518,10 @@ fa_status launch(const void* q, const void* k, const void* v, const void* o, con
   }
   bwd_delta_kernel<D><<<static_cast<unsigned>((rows + 255) / 256), 256, 0, stream>>>(
       static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dout), delta, rows);
-  CUtensorMap tq, tk, tv, tdo;
+  CUtensorMap tq, tk, tv, tdo, tdq;
   if (!encode_bf16_map(&tq, q, D, N, bh, 128) || !encode_bf16_map(&tk, k, D, N, bh, 128) ||
-      !encode_bf16_map(&tv, v, D, N, bh, 128) || !encode_bf16_map(&tdo, dout, D, N, bh, 128))
+      !encode_bf16_map(&tv, v, D, N, bh, 128) || !encode_bf16_map(&tdo, dout, D, N, bh, 128) ||
+      !encode_f32_map(&tdq, dq_acc, D, N, bh, 128))
     return FA_ERR_CUDA;
   BwdParams prm;
   prm.lse = lse;
@@ -373,7 +541,7 @@ fa_status launch(const void* q, const void* k, const void* v, const void* o, con
     return FA_ERR_CUDA;
   }
   dim3 grid(static_cast<unsigned>(bh), static_cast<unsigned>(prm.num_kv_tiles));
-  bwd_kernel<D><<<grid, kBwdThreads, C::kSmemBytes, stream>>>(tq, tk, tv, tdo, prm);
+  bwd_kernel<D><<<grid, kBwdThreads, C::kSmemBytes, stream>>>(tq, tk, tv, tdo, tdq, prm);
   const long long n4 = rows * D / 4;
   bwd_dq_convert_kernel<<<static_cast<unsigned>((n4 + 255) / 256), 256, 0, stream>>>(
       dq_acc, static_cast<__nv_bfloat16*>(dq), n4);

@@ -14,6 +14,9 @@ namespace fa {
 // box and 128-byte swizzle. Returns false (and sets the error text) on failure.
 bool encode_bf16_map(CUtensorMap* map, const void* base, uint64_t d, uint64_t rows, uint64_t outer,
                      uint32_t box_rows);
+// The same over fp32 elements with a {32, box_rows, 1} box (128-byte rows).
+bool encode_f32_map(CUtensorMap* map, const void* base, uint64_t d, uint64_t rows, uint64_t outer,
+                    uint32_t box_rows);
 
 // Record the text of a CUDA failure for fa_last_error_string.
 void set_error_text(const char* what, cudaError_t err);

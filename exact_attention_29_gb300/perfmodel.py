@@ -10,6 +10,11 @@ rows and K/V re-read once per Q tile: 2Nd (read Q, write O) + 2Nd * N/B_r
 "已有的几种大模型上下文支持情况" §3.3). When K/V stay in L2 the re-reads
 collapse to one read, leaving the algorithmic minimum 4Nd + N.
 
+The backward with recomputation (Lecture 5 notes §7.2-7.3) makes five
+N x N x d products per head: S = Q K^T again, dP = dO V^T, dV = P^T dO,
+dK = dS^T Q and dQ = dS K, 10 N^2 d FLOPs, half under the causal mask (a
+count derived from those products; the pages print no figure for it).
+
 Decode reads every cached K and V element of every visible position once
 (arithmetic intensity about 1, Lecture 5 notes §8.3).
 """
@@ -18,6 +23,11 @@ from __future__ import annotations
 
 def fwd_flops(B: int, H: int, N: int, d: int, causal: bool) -> float:
     f = 4.0 * B * H * N * N * d
+    return f / 2 if causal else f
+
+
+def bwd_flops(B: int, H: int, N: int, d: int, causal: bool) -> float:
+    f = 10.0 * B * H * N * N * d
     return f / 2 if causal else f
 
 

@@ -2,6 +2,7 @@
 
     python -m exact_attention_29_gb300.run_case --workload llama3_8b_prefill --iters 3
     python -m exact_attention_29_gb300.run_case --workload decode_32k --batch 4 --splits 16 --iters 3
+    python -m exact_attention_29_gb300.run_case --workload llama3_8b_prefill --bwd --iters 3
 
 ``--batch`` overrides B (to keep a profiled case small); inputs are drawn by
 the seeded generators of ``workloads.py``. Prints the device time per
@@ -30,6 +31,7 @@ def main():
     ap.add_argument("--iters", type=int, default=3)
     ap.add_argument("--batch", type=int, default=0)
     ap.add_argument("--splits", type=int, default=16)
+    ap.add_argument("--bwd", action="store_true", help="time fa_bwd (after one fa_fwd) on a prefill workload")
     args = ap.parse_args()
     build.build()
     dev = torch.device("cuda:0")
@@ -43,6 +45,14 @@ def main():
 
         def run():
             fa.fa_fwd(q, k, v, causal=c.causal, o=o, lse=lse, stream=stream)
+
+        if args.bwd:
+            run()
+            do = wl.backward_inputs(B, c.H, c.N, c.d, seed=0, device=dev)
+            dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
+
+            def run():
+                fa.fa_bwd(q, k, v, o, lse, do, causal=c.causal, dq=dq, dk=dk, dv=dv, stream=stream)
     else:
         c = wl.DECODE[args.workload]
         B = args.batch or c.B
@@ -64,7 +74,15 @@ def main():
         torch.cuda.synchronize(dev)
         times.append(e0.elapsed_time(e1))
     fa.fa_check_device_error(stream)
-    print(f"{args.workload} B={B}: " + " ".join(f"{t:.3f}ms" for t in times))
+    extra = ""
+    if args.workload in wl.PREFILL:
+        from exact_attention_29_gb300 import perfmodel
+
+        flops = (perfmodel.bwd_flops if args.bwd else perfmodel.fwd_flops)(B, c.H, c.N, c.d, c.causal)
+        extra = f" best {flops / min(times) / 1e9:.1f} TFLOP/s"
+    what = "bwd" if args.bwd else "fwd"
+    print(f"{args.workload} {what if args.workload in wl.PREFILL else ''} B={B}: "
+          + " ".join(f"{t:.3f}ms" for t in times) + extra)
 
 
 if __name__ == "__main__":
