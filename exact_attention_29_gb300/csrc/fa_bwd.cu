@@ -63,9 +63,8 @@ struct BwdCfg {
   static constexpr int kQOff = 2 * kTileBytes;  // two buffers
   static constexpr int kDoOff = 4 * kTileBytes;
   static constexpr int kDsOff = 5 * kTileBytes;
-  static constexpr int kBoxBytes = 128 * 32 * 4;      // one dQ staging box: 128 rows x 32 fp32
-  static constexpr int kStageOff = kDsOff + kDsBytes;  // third staging box (d = 128)
-  static constexpr int kVecOff = kStageOff + kBoxBytes;  // [2][128] L log2 e, then [2][128] D
+  static constexpr int kBoxBytes = 128 * 32 * 4;  // d = 64 dQ staging: 128 rows x 32 fp32 (4 warps' boxes)
+  static constexpr int kVecOff = kDsOff + kDsBytes;  // [2][128] L log2 e, then [2][128] D
   static constexpr int kBarOff = kVecOff + 4 * 128 * 4;
   static constexpr int kSmemBytes = kBarOff + 256 + 1024;
   static constexpr uint32_t kColS = 0, kColDp = 128, kColDv = 256, kColDk = 384;
@@ -86,7 +85,8 @@ enum BwdBar : int {
   kBarDq = 13,
   kBarDqEmpty = 14,
   kBarAcc = 15,
-  kNumBars = 16,
+  kBarStageFree = 16,  // the read-out's reductions have read the dS^T buffer
+  kNumBars = 17,
 };
 
 struct BwdParams {
@@ -138,6 +138,10 @@ __global__ void __launch_bounds__(256) bwd_dq_convert_kernel(const float* __rest
   reinterpret_cast<uint2*>(dq)[i] = w;
 }
 
+__device__ __forceinline__ void red_add_f32(float* addr, float a) {
+  asm volatile("red.global.add.f32 [%0], %1;" ::"l"(addr), "f"(a) : "memory");
+}
+
 template <int D>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -151,7 +155,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   uint8_t* sq = base + C::kQOff;
   uint8_t* sdo = base + C::kDoOff;
   uint8_t* sds = base + C::kDsOff;
-  uint8_t* sstage = base + C::kStageOff;
   float* vec_l = reinterpret_cast<float*>(base + C::kVecOff);  // [2][128]
   float* vec_d = vec_l + 256;                                  // [2][128]
   uint64_t* bars = reinterpret_cast<uint64_t*>(base + C::kBarOff);
@@ -186,6 +189,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     mbar_init(&bars[kBarDq], 1);
     mbar_init(&bars[kBarDqEmpty], 4);
     mbar_init(&bars[kBarAcc], 1);
+    mbar_init(&bars[kBarStageFree], 4);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -290,7 +294,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         tc_fence_after();
         issue_pv<D>(tmem + C::kColDk, dp_tm, smem_u32(sq + b * C::kTileBytes), it > 0, 32);
         umma_commit(&bars[kBarQEmpty + b]);
-        issue_mn_mn<D>(dp_tm, smem_u32(sds), smem_u32(sk));
+        if constexpr (D == 128) {
+          // dQ^T = K^T dS^T: d on the TMEM lanes, so that each read-out warp
+          // instruction adds one whole 128-byte segment of a dQ row
+          issue_mn_mn<128>(dp_tm, smem_u32(sk), smem_u32(sds));
+        } else {
+          issue_mn_mn<D>(dp_tm, smem_u32(sds), smem_u32(sk));
+        }
         umma_commit(&bars[kBarDq]);
         // dP of the next tile once the dQ share has been read out
         if (more) {
@@ -378,6 +388,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         break;
       }
       tc_fence_after();
+      // the dS^T buffer held dQ boxes of the previous tile: their reads must be done
+      if (D == 64 && it > 0) {
+        ok = bounded_wait(&bars[kBarStageFree], (it - 1) & 1, abort_flag, p.err, kSiteOEmpty);
+        if (!__all_sync(kFull, ok)) {
+          ok = false;
+          break;
+        }
+      }
       const float4* d4 = reinterpret_cast<const float4*>(vec_d + b * 128 + 64 * half);
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
@@ -444,55 +462,83 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
   } else {
     // ---------------------------------------------------------------- dQ read-out
-    // warp w owns query rows 32w.. of the dQ share. Each 32-column slice of
-    // dQ goes (scaled) into a shared-memory box in the tensor map's swizzled
-    // layout and one thread adds the box into the fp32 accumulator with a
-    // bulk tensor reduction; rows beyond N are clipped by the map.
-    // Boxes: slices 0 and 1 in the two halves of the dS^T buffer (free once
-    // the dQ product is complete and until the next dS is written, which
-    // waits for dq_empty), slice 2 in its own box, slice 3 in the first half
-    // again.
-    const int row = warp * 32 + lane;
+    // d = 128: the share is dQ^T (lane = column d of dQ, TMEM column = query
+    // row). Each warp instruction adds 32 consecutive floats (one 128-byte
+    // segment) of one dQ row with a plain reduction; the TMEM columns are
+    // released as soon as the last slice has been loaded.
+    // d = 64: the share is dQ (lane = query row); warp w owns rows 32w.. and
+    // stages its two 32-column slices (scaled) into 4 KB shared-memory boxes
+    // in the tensor map's swizzled layout; lane 0 adds each box into the fp32
+    // accumulator with a bulk tensor reduction (rows beyond N are clipped by
+    // the map). The boxes lie in the two halves of the dS^T buffer, free once
+    // the dQ product is complete and until the P/dS warps write the next dS^T,
+    // which they do after kBarStageFree.
     const uint32_t dq_tm = tmem + (static_cast<uint32_t>(warp * 32) << 16) + C::kColDp;
-    const bool issuer = tid == 0;
-    if (issuer) tma_prefetch_desc(&tm_dq);
-    for (int it = 0; it < n_it; ++it) {
-      bool ok = bounded_wait(&bars[kBarDq], it & 1, abort_flag, p.err, kSitePFull);
-      // one decision for all four warps: they meet at named barriers below
-      if (!named_bar_and(1, 128, ok)) break;
-      tc_fence_after();
-      const int q0 = (i_first + it) * 128;
+    if constexpr (D == 128) {
+      const int dcol = warp * 32 + lane;
+      for (int it = 0; it < n_it; ++it) {
+        const bool ok = bounded_wait(&bars[kBarDq], it & 1, abort_flag, p.err, kSitePFull);
+        if (!__all_sync(kFull, ok)) break;
+        tc_fence_after();
+        const int q0 = (i_first + it) * 128;
+        const int nq = min(128, p.N - q0);
+        float* dst = p.dq_acc + (head_rows + q0) * D + dcol;
 #pragma unroll 1
-      for (int c = 0; c < D / 32; ++c) {
-        uint8_t* box = (c == 2) ? sstage : sds + (c == 1 ? C::kBoxBytes : 0);
-        if (c == 3) {
-          // slice 0's reduction must have finished reading the first half
-          if (issuer) bulk_wait_group_read<2>();
-          named_bar_sync(1, 128);
-        }
-        uint32_t r[32];
-        tmem_ld_x32(dq_tm + 32 * c, r);
-        uint8_t* rowp = box + row * 128;
+        for (int c = 0; c < 128; c += 32) {
+          uint32_t r[32];
+          tmem_ld_x32(dq_tm + c, r);
+          if (c == 96) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars[kBarDqEmpty]);
+          }
+          if (c + 32 <= nq) {
 #pragma unroll
-        for (int u = 0; u < 8; ++u)
-          *reinterpret_cast<float4*>(rowp + ((u ^ (row & 7)) << 4)) =
-              make_float4(__uint_as_float(r[4 * u]) * p.scale, __uint_as_float(r[4 * u + 1]) * p.scale,
-                          __uint_as_float(r[4 * u + 2]) * p.scale, __uint_as_float(r[4 * u + 3]) * p.scale);
-        fence_proxy_async_smem();
-        named_bar_sync(1, 128);
-        if (issuer) {
-          tma_reduce_add_3d(&tm_dq, box, 32 * c, q0, bh);
-          bulk_commit_group();
+            for (int e = 0; e < 32; ++e) red_add_f32(dst + static_cast<size_t>(c + e) * D, __uint_as_float(r[e]) * p.scale);
+          } else {
+#pragma unroll
+            for (int e = 0; e < 32; ++e)
+              if (c + e < nq) red_add_f32(dst + static_cast<size_t>(c + e) * D, __uint_as_float(r[e]) * p.scale);
+          }
         }
       }
-      // the dS^T buffer is written again after the next dP: its reads must be done
-      if (issuer) bulk_wait_group_read<0>();
-      tc_fence_before();
-      named_bar_sync(1, 128);
-      if (lane == 0) mbar_arrive(&bars[kBarDqEmpty]);
+    } else {
+      static_assert(D == 64, "one 64-column pair");
+      if (lane == 0 && warp == 0) tma_prefetch_desc(&tm_dq);
+      for (int it = 0; it < n_it; ++it) {
+        const bool ok = bounded_wait(&bars[kBarDq], it & 1, abort_flag, p.err, kSitePFull);
+        if (!__all_sync(kFull, ok)) break;
+        tc_fence_after();
+        const int q0 = (i_first + it) * 128;
+        uint32_t r[64];
+        tmem_ld_x64(dq_tm, r);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars[kBarDqEmpty]);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          uint8_t* rowp = sds + h * C::kBoxBytes + warp * 4096 + lane * 128;
+#pragma unroll
+          for (int u = 0; u < 8; ++u)
+            *reinterpret_cast<float4*>(rowp + ((u ^ (lane & 7)) << 4)) = make_float4(
+                __uint_as_float(r[32 * h + 4 * u]) * p.scale, __uint_as_float(r[32 * h + 4 * u + 1]) * p.scale,
+                __uint_as_float(r[32 * h + 4 * u + 2]) * p.scale, __uint_as_float(r[32 * h + 4 * u + 3]) * p.scale);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_reduce_add_3d(&tm_dq, sds + h * C::kBoxBytes + warp * 4096, 32 * h, q0 + 32 * warp, bh);
+            bulk_commit_group();
+          }
+        }
+        if (lane == 0) {
+          bulk_wait_group_read<0>();
+          mbar_arrive(&bars[kBarStageFree]);
+        }
+        __syncwarp();
+      }
+      // the additions must be complete before the CTA exits
+      if (lane == 0) bulk_wait_group<0>();
     }
-    // the additions must be complete before the CTA exits
-    if (issuer) bulk_wait_group<0>();
   }
 
   tc_fence_before();
@@ -521,7 +567,7 @@ fa_status launch(const void* q, const void* k, const void* v, const void* o, con
   CUtensorMap tq, tk, tv, tdo, tdq;
   if (!encode_bf16_map(&tq, q, D, N, bh, 128) || !encode_bf16_map(&tk, k, D, N, bh, 128) ||
       !encode_bf16_map(&tv, v, D, N, bh, 128) || !encode_bf16_map(&tdo, dout, D, N, bh, 128) ||
-      !encode_f32_map(&tdq, dq_acc, D, N, bh, 128))
+      !encode_f32_map(&tdq, dq_acc, D, N, bh, 32))
     return FA_ERR_CUDA;
   BwdParams prm;
   prm.lse = lse;
