@@ -17,6 +17,7 @@ from ._lib import (  # noqa: F401
     fa_bwd_plan,
     fa_check_device_error,
     fa_decode,
+    fa_decode_gqa,
     fa_decode_noalloc,
     fa_fwd,
     fa_fwd_plan,

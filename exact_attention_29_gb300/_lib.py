@@ -32,6 +32,7 @@ _SIGNATURES = {
     "fa_fwd": ([_VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, ctypes.c_float, _VP], _I),
     "fa_decode": ([_VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _VP], _I),
     "fa_bwd": ([_VP] * 9 + [_I] * 5 + [ctypes.c_float, _VP], _I),
+    "fa_decode_gqa": ([_VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _I, _VP], _I),
     "fa_bwd_plan": ([_I, _I, _I, _I, ctypes.POINTER(ctypes.c_longlong)], _I),
     "fa_decode_noalloc": ([_VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _VP], _I),
     "fa_status_string": ([_I], ctypes.c_char_p),
@@ -185,6 +186,37 @@ def fa_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, seq
     st = lib.fa_decode(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), seqlens.data_ptr(), o.data_ptr(),
                        lse.data_ptr(), B, H, L, d, int(num_splits), _stream_handle(stream))
     _check(st, "fa_decode")
+    return o, lse
+
+
+def fa_decode_gqa(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, seqlens: torch.Tensor,
+                  num_splits: int, o: torch.Tensor | None = None, lse: torch.Tensor | None = None, stream=None):
+    """Flash-Decoding with grouped K/V heads. q bf16 [B, Hq, d]; caches bf16
+    [B, Hkv, L, d] with Hq a multiple of Hkv (query head h uses K/V head
+    h // (Hq // Hkv)); seqlens int32 [B] on the GPU.
+
+    Returns (o bf16 [B, Hq, d], lse fp32 [B, Hq]).
+    """
+    lib = load_library()
+    _require(q, "q", torch.bfloat16, 3)
+    _require(k_cache, "k_cache", torch.bfloat16, 4)
+    _require(v_cache, "v_cache", torch.bfloat16, 4)
+    _require(seqlens, "seqlens", torch.int32, 1)
+    B, Hkv, L, d = k_cache.shape
+    Hq = q.shape[1]
+    if v_cache.shape != k_cache.shape or q.shape != (B, Hq, d) or seqlens.shape != (B,):
+        raise ValueError("shapes must be q [B,Hq,d], caches [B,Hkv,L,d], seqlens [B]")
+    if Hq % Hkv != 0:
+        raise ValueError("Hq must be a multiple of Hkv")
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+    _require(o, "o", torch.bfloat16, 3)
+    _require(lse, "lse", torch.float32, 2)
+    st = lib.fa_decode_gqa(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), seqlens.data_ptr(), o.data_ptr(),
+                           lse.data_ptr(), B, Hq, Hkv, L, d, int(num_splits), _stream_handle(stream))
+    _check(st, "fa_decode_gqa")
     return o, lse
 
 

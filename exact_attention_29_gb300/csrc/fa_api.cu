@@ -220,6 +220,43 @@ fa_status fa_decode(const void* q, const void* k_cache, const void* v_cache, con
   return st;
 }
 
+fa_status fa_decode_gqa(const void* q, const void* k_cache, const void* v_cache, const int32_t* seqlens, void* o,
+                        float* lse, int B, int Hq, int Hkv, int L, int d, int num_splits, fa_stream_t stream) {
+  if (!q || !k_cache || !v_cache || !seqlens || !o || !lse) return FA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned4(seqlens) || !aligned4(o) ||
+      !aligned4(lse))
+    return FA_ERR_INVALID_ARG;
+  if (B < 1 || Hq < 1 || Hkv < 1 || L < 1 || d < 1 || Hq % Hkv != 0) return FA_ERR_INVALID_ARG;
+  if (num_splits < 1 || num_splits > 64) return FA_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  const long long groups = (Hq / Hkv + 15) / 16;
+  if (B > 65535 || static_cast<long long>(Hkv) * groups > 65535 || static_cast<long long>(B) * Hq > 0x7fffffffLL)
+    return FA_ERR_INVALID_ARG;
+  int dev = -1;
+  fa_status st = current_device(&dev);
+  if (st != FA_OK) return st;
+  unsigned int* err = device_error_word();
+  if (!err) return FA_ERR_CUDA;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const size_t parts = static_cast<size_t>(B) * Hq * num_splits;
+  void* ws = nullptr;
+  cudaError_t e = cudaMallocAsync(&ws, parts * (d + 1) * sizeof(float), s);
+  if (e != cudaSuccess) {
+    set_error_text("cudaMallocAsync(decode workspace)", e);
+    return FA_ERR_CUDA;
+  }
+  float* ws_o = static_cast<float*>(ws);
+  float* ws_lse = ws_o + parts * d;
+  st = launch_decode_gqa_split(q, k_cache, v_cache, seqlens, B, Hq, Hkv, L, d, num_splits, ws_o, ws_lse, s, err);
+  if (st == FA_OK) st = launch_decode_merge(ws_o, ws_lse, o, lse, static_cast<long long>(B) * Hq, d, num_splits, s);
+  e = cudaFreeAsync(ws, s);
+  if (st == FA_OK && e != cudaSuccess) {
+    set_error_text("cudaFreeAsync(decode workspace)", e);
+    st = FA_ERR_CUDA;
+  }
+  return st;
+}
+
 fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
                  void* dq, void* dk, void* dv, int B, int H, int N, int d, int causal, float scale, fa_stream_t stream) {
   if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv) return FA_ERR_INVALID_ARG;

@@ -237,6 +237,24 @@ fa_status launch(const void* q, const void* k_cache, const void* v_cache, const 
 
 }  // namespace
 
+fa_status launch_decode_merge(const float* ws_o, const float* ws_lse, void* o, float* lse, long long heads, int d,
+                              int num_splits, cudaStream_t stream) {
+  if (d == 128)
+    decode_merge_kernel<128><<<static_cast<unsigned>(heads), 128, 0, stream>>>(
+        ws_o, ws_lse, static_cast<__nv_bfloat16*>(o), lse, num_splits);
+  else if (d == 64)
+    decode_merge_kernel<64><<<static_cast<unsigned>(heads), 64, 0, stream>>>(
+        ws_o, ws_lse, static_cast<__nv_bfloat16*>(o), lse, num_splits);
+  else
+    return FA_ERR_UNSUPPORTED;
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) {
+    set_error_text("decode_merge_kernel launch", e);
+    return FA_ERR_CUDA;
+  }
+  return FA_OK;
+}
+
 fa_status launch_decode(const void* q, const void* k_cache, const void* v_cache, const int32_t* seqlens, void* o,
                         float* lse, int B, int H, int L, int d, int num_splits, float* ws_o, float* ws_lse,
                         cudaStream_t stream) {

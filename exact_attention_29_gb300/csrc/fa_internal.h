@@ -33,6 +33,15 @@ fa_status launch_decode(const void* q, const void* k_cache, const void* v_cache,
                         float* lse, int B, int H, int L, int d, int num_splits, float* ws_o, float* ws_lse,
                         cudaStream_t stream);
 
+// The log-sum-exp merge of fa_decode over `heads` (batch, head) rows of partials.
+fa_status launch_decode_merge(const float* ws_o, const float* ws_lse, void* o, float* lse, long long heads, int d,
+                              int num_splits, cudaStream_t stream);
+
+// The GQA split kernel: partials of [B][Hq][num_splits] into ws_o / ws_lse.
+fa_status launch_decode_gqa_split(const void* q, const void* k_cache, const void* v_cache, const int32_t* seqlens,
+                                  int B, int Hq, int Hkv, int L, int d, int num_splits, float* ws_o, float* ws_lse,
+                                  cudaStream_t stream, unsigned int* err);
+
 // dq_acc: fp32 [B*H*N*d] scratch (zeroed by the call), delta: fp32 [B*H*N] scratch.
 fa_status launch_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
                      void* dq, void* dk, void* dv, int B, int H, int N, int d, int causal, float scale, float* dq_acc,

@@ -27,7 +27,8 @@ def main():
     from exact_attention_29_gb300 import workloads as wl
 
     ap = argparse.ArgumentParser()
-    ap.add_argument("--workload", required=True, choices=sorted(list(wl.PREFILL) + list(wl.DECODE)))
+    ap.add_argument("--workload", required=True,
+                    choices=sorted(list(wl.PREFILL) + list(wl.DECODE) + list(wl.DECODE_GQA)))
     ap.add_argument("--iters", type=int, default=3)
     ap.add_argument("--batch", type=int, default=0)
     ap.add_argument("--splits", type=int, default=16)
@@ -53,7 +54,7 @@ def main():
 
             def run():
                 fa.fa_bwd(q, k, v, o, lse, do, causal=c.causal, dq=dq, dk=dk, dv=dv, stream=stream)
-    else:
+    elif args.workload in wl.DECODE:
         c = wl.DECODE[args.workload]
         B = args.batch or c.B
         q, kc, vc, sl = wl.decode_inputs(B, c.H, c.L, c.d, seed=0, ragged=c.ragged, device=dev)
@@ -62,6 +63,15 @@ def main():
 
         def run():
             fa.fa_decode(q, kc, vc, sl, args.splits, o=o, lse=lse, stream=stream)
+    else:
+        c = wl.DECODE_GQA[args.workload]
+        B = args.batch or c.B
+        q, kc, vc, sl = wl.decode_gqa_inputs(B, c.Hq, c.Hkv, c.L, c.d, seed=0, ragged=c.ragged, device=dev)
+        o = torch.empty_like(q)
+        lse = torch.empty((B, c.Hq), dtype=torch.float32, device=dev)
+
+        def run():
+            fa.fa_decode_gqa(q, kc, vc, sl, args.splits, o=o, lse=lse, stream=stream)
 
     torch.cuda.synchronize(dev)
     times = []
@@ -80,6 +90,11 @@ def main():
 
         flops = (perfmodel.bwd_flops if args.bwd else perfmodel.fwd_flops)(B, c.H, c.N, c.d, c.causal)
         extra = f" best {flops / min(times) / 1e9:.1f} TFLOP/s"
+    else:
+        from exact_attention_29_gb300 import perfmodel
+
+        kv = perfmodel.decode_kv_bytes(c.Hkv if hasattr(c, "Hkv") else c.H, c.d, sl.tolist())
+        extra = f" best {kv / min(times) / 1e6:.0f} GB/s of K/V"
     what = "bwd" if args.bwd else "fwd"
     print(f"{args.workload} {what if args.workload in wl.PREFILL else ''} B={B}: "
           + " ".join(f"{t:.3f}ms" for t in times) + extra)

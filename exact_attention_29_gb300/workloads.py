@@ -78,6 +78,32 @@ DECODE = {
 DECODE_SPLITS = (8, 16, 32)
 
 
+@dataclass(frozen=True)
+class DecodeGQA:
+    name: str
+    B: int
+    Hq: int
+    Hkv: int
+    L: int
+    d: int
+    ragged: bool
+
+    @property
+    def g(self) -> int:
+        return self.Hq // self.Hkv
+
+
+# Grouped K/V heads (Lecture 5 notes, Exercise 7): g = 8 is the 64-query-head,
+# 8-K/V-head grouping the exercise takes; g = 4 groups 32 query heads over 8
+# K/V heads; MQA puts 32 query heads on one K/V head.
+DECODE_GQA = {
+    "decode_gqa8_32k": DecodeGQA("decode_gqa8_32k", 16, 64, 8, 32768, 128, False),
+    "decode_gqa8_32k_ragged": DecodeGQA("decode_gqa8_32k_ragged", 16, 64, 8, 32768, 128, True),
+    "decode_gqa4_32k": DecodeGQA("decode_gqa4_32k", 16, 32, 8, 32768, 128, False),
+    "decode_mqa_32k": DecodeGQA("decode_mqa_32k", 16, 32, 1, 32768, 128, False),
+}
+
+
 def _randn_bf16(shape, gen: torch.Generator, device) -> torch.Tensor:
     numel = 1
     for s in shape:
@@ -121,6 +147,23 @@ def decode_inputs(B: int, H: int, L: int, d: int, seed: int = 0, ragged: bool = 
     q = _randn_bf16((B, H, d), g, device)
     k = _randn_bf16((B, H, L, d), g, device)
     v = _randn_bf16((B, H, L, d), g, device)
+    if ragged:
+        gl = torch.Generator(device="cpu")
+        gl.manual_seed(seed + 1)
+        seqlens = torch.randint(min(lo, L), L + 1, (B,), generator=gl, dtype=torch.int64).to(torch.int32)
+    else:
+        seqlens = torch.full((B,), L, dtype=torch.int32)
+    return q, k, v, seqlens.to(device)
+
+
+def decode_gqa_inputs(B: int, Hq: int, Hkv: int, L: int, d: int, seed: int = 0, ragged: bool = False,
+                      device="cpu", lo: int = 1024):
+    """q [B,Hq,d], K/V caches [B,Hkv,L,d] (bf16) and seqlens [B] (int32), drawn
+    in that order; lengths as in decode_inputs."""
+    g = _generator(seed, B * Hkv * L * d, device)
+    q = _randn_bf16((B, Hq, d), g, device)
+    k = _randn_bf16((B, Hkv, L, d), g, device)
+    v = _randn_bf16((B, Hkv, L, d), g, device)
     if ragged:
         gl = torch.Generator(device="cpu")
         gl.manual_seed(seed + 1)

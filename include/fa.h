@@ -8,7 +8,9 @@
  *              probability matrices never reach device memory.
  *   fa_decode  Flash-Decoding: one query token per (batch, head) against a long
  *              KV cache, split along the keys, the per-split summaries merged
- *              by the log-sum-exp combine.
+ *              by the log-sum-exp combine (fa_decode_gqa: query heads grouped
+ *              over shared K/V heads).
+ *   fa_bwd     gradients of fa_fwd, recomputing P from the saved log-sum-exp.
  *
  * Conventions for every call:
  *   - Tensor arguments are DEVICE pointers (memory of the current CUDA device),
@@ -125,6 +127,28 @@ fa_status fa_bwd_plan(int N, int d, int block, int causal, long long *dq_atomic_
  */
 fa_status fa_decode(const void *q, const void *k_cache, const void *v_cache, const int32_t *seqlens, void *o,
                     float *lse, int B, int H, int L, int d, int num_splits, fa_stream_t stream);
+
+/*
+ * Decode attention with grouped K/V heads (GQA; MQA when H_kv = 1).
+ *
+ * Defines: CMU 15-779 Lecture 5 notes, Exercise 7 (g = H_q / H_kv query heads
+ *   share one K/V head, so each K/V element read serves g queries and the
+ *   arithmetic intensity of decode rises to about g) and §8.4 (the split
+ *   along the keys and the log-sum-exp merge, as fa_decode).
+ *
+ *   q        bf16 [B][H_q][d].
+ *   k_cache, v_cache  bf16 [B][H_kv][L][d].
+ *   Query head h attends to K/V head h / (H_q / H_kv): the g consecutive query
+ *   heads h_kv*g .. h_kv*g + g - 1 share K/V head h_kv.
+ *   seqlens, o [B][H_q][d], lse [B][H_q], d, num_splits: as fa_decode
+ *   (keys of a sequence are cut into num_splits chunks of ceil(len/num_splits)
+ *   rounded up to a multiple of 128 keys). H_q must be a multiple of H_kv.
+ *   Cache entries at or beyond seqlens[b] may hold any bits (NaN included).
+ * Workspace: B*H_q*num_splits*(d+1)*4 bytes of stream-ordered device memory.
+ * Errors: as fa_decode; FA_ERR_INVALID_ARG also when H_q % H_kv != 0.
+ */
+fa_status fa_decode_gqa(const void *q, const void *k_cache, const void *v_cache, const int32_t *seqlens, void *o,
+                        float *lse, int B, int Hq, int Hkv, int L, int d, int num_splits, fa_stream_t stream);
 
 /*
  * Decode attention that allocates nothing.

@@ -68,6 +68,8 @@ def _load():
             lib.oracle_attention.restype = ctypes.c_int
             lib.oracle_decode.argtypes = [dp, dp, dp, ip, dp, dp] + [ctypes.c_int] * 4
             lib.oracle_decode.restype = ctypes.c_int
+            lib.oracle_decode_gqa.argtypes = [dp, dp, dp, ip, dp, dp] + [ctypes.c_int] * 5
+            lib.oracle_decode_gqa.restype = ctypes.c_int
             lib.oracle_attention_bwd.argtypes = [dp] * 7 + [ctypes.c_int] * 5 + [ctypes.c_double]
             lib.oracle_attention_bwd.restype = ctypes.c_int
             _lib = lib
@@ -161,6 +163,29 @@ def decode(q, k_cache, v_cache, seqlens):
     rc = lib.oracle_decode(_ptr(qq), _ptr(kk), _ptr(vv), _ptr(sl, ctypes.c_int), _ptr(o), _ptr(lse),
                            B, H, L, d)
     _check(rc, "decode")
+    return o, lse
+
+
+def decode_gqa(q, k_cache, v_cache, seqlens):
+    """Decode with grouped K/V heads: q [B,Hq,d], caches [B,Hkv,L,d], Hq a
+    multiple of Hkv; query head h uses K/V head h // (Hq // Hkv).
+
+    Returns (o [B,Hq,d], lse [B,Hq]).
+    """
+    lib = _load()
+    qq, kk, vv = _f64(q), _f64(k_cache), _f64(v_cache)
+    B, Hkv, L, d = kk.shape
+    if qq.ndim != 3 or qq.shape[0] != B or qq.shape[2] != d or vv.shape != kk.shape:
+        raise ValueError("q must be [B,Hq,d] and the caches [B,Hkv,L,d]")
+    Hq = qq.shape[1]
+    if hasattr(seqlens, "detach"):
+        seqlens = seqlens.detach().cpu().numpy()
+    sl = np.ascontiguousarray(np.asarray(seqlens, dtype=np.int32))
+    o = np.empty((B, Hq, d), dtype=np.float64)
+    lse = np.empty((B, Hq), dtype=np.float64)
+    rc = lib.oracle_decode_gqa(_ptr(qq), _ptr(kk), _ptr(vv), _ptr(sl, ctypes.c_int), _ptr(o), _ptr(lse),
+                               B, Hq, Hkv, L, d)
+    _check(rc, "decode_gqa")
     return o, lse
 
 

@@ -195,6 +195,39 @@ int oracle_decode(const double *q, const double *k_cache, const double *v_cache,
 }
 
 /*
+ * Decode with grouped K/V heads (GQA; MQA when H_kv = 1).
+ *
+ *   q [B][H_q][d]; k_cache, v_cache [B][H_kv][L][d]; seqlens [B];
+ *   o [B][H_q][d]; lse [B][H_q]. H_q must be a multiple of H_kv.
+ *
+ * CMU 15-779 Lecture 5 notes, Exercise 7 (and §8.3): g = H_q / H_kv query
+ * heads share one K/V head. Query head h attends to K/V head h / g (the g
+ * consecutive query heads h_kv*g .. h_kv*g + g - 1 form one group), over
+ * keys 0..seqlens[b]-1, unmasked, scale 1/sqrt(d), exactly as a decode step
+ * with its own K/V head would.
+ */
+int oracle_decode_gqa(const double *q, const double *k_cache, const double *v_cache,
+                      const int *seqlens, double *o, double *lse, int B, int Hq,
+                      int Hkv, int L, int d) {
+  if (B < 1 || Hq < 1 || Hkv < 1 || L < 1 || d < 1 || Hq % Hkv != 0) return ORACLE_ERR_ARG;
+  int g = Hq / Hkv;
+  double scale = 1.0 / sqrt((double)d);
+  for (int b = 0; b < B; ++b) {
+    int len = seqlens[b];
+    if (len < 1 || len > L) return ORACLE_ERR_ARG;
+    for (int h = 0; h < Hq; ++h) {
+      size_t bq = (size_t)b * Hq + h;
+      size_t bkv = (size_t)b * Hkv + h / g;
+      int rc = oracle_attention_rows(q + bq * d, NULL, k_cache + bkv * (size_t)L * d,
+                                     v_cache + bkv * (size_t)L * d, 1, len, d, 0,
+                                     scale, o + bq * d, lse + bq, NULL, NULL);
+      if (rc != ORACLE_OK) return rc;
+    }
+  }
+  return ORACLE_OK;
+}
+
+/*
  * Backward of standard attention for one (batch, head), every intermediate
  * materialised, fp64.
  *

@@ -178,3 +178,18 @@ def test_bwd_rejects_bad_arguments(lib):
     assert bwd(scale=-1.0) == fa.FA_ERR_INVALID_ARG
     assert bwd(causal=3) == fa.FA_ERR_INVALID_ARG
     assert bwd(d=96) == fa.FA_ERR_UNSUPPORTED
+
+
+def test_decode_gqa_rejects_bad_arguments(lib):
+    import exact_attention_29_gb300 as fa
+
+    def dec(Hq=8, Hkv=2, num_splits=4, d=128, L=64, q=16):
+        return lib.fa_decode_gqa(q, 16, 16, 16, 16, 16, 1, Hq, Hkv, L, d, num_splits, None)
+
+    assert dec(Hq=6, Hkv=4) == fa.FA_ERR_INVALID_ARG
+    assert dec(Hkv=0) == fa.FA_ERR_INVALID_ARG
+    assert dec(num_splits=0) == fa.FA_ERR_INVALID_ARG
+    assert dec(num_splits=65) == fa.FA_ERR_INVALID_ARG
+    assert dec(q=None) == fa.FA_ERR_INVALID_ARG
+    assert dec(L=0) == fa.FA_ERR_INVALID_ARG
+    assert dec(d=96) == fa.FA_ERR_UNSUPPORTED
