@@ -19,10 +19,13 @@
 //   O^T += V^T P^T   M = d (TMEM lanes; d = 64 is padded to 128 with a zero
 //                     block of shared memory), N = 16, K = 128 keys; A = V
 //                     MN-major, B = P^T K-major in shared memory
-// Warps 0-3 do the softmax, the O rescale and the epilogue, warp 4 issues the
-// TMA copies of K and V (a ring of stages), warp 5 issues the products. The
-// partials (o/l, m + log2 l) go to the same workspace layout the merge kernel
-// of fa_decode.cu reads. Every wait is bounded (fa_common.cuh).
+// Two softmax warpgroups (warps 0-3 and 4-7) take alternate key tiles, each
+// with its own running (m, l) and its own O^T accumulator, so one group's
+// softmax overlaps the other's; at the end the two summaries are merged with
+// the combine operator of §4.4-4.5. Warp 8 issues the TMA copies of K and V (a
+// ring of stages), warp 9 issues the products. The partials (o/l, m + log2 l)
+// go to the same workspace layout the merge kernel of fa_decode.cu reads.
+// Every wait is bounded (fa_common.cuh).
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -35,9 +38,9 @@
 namespace fa {
 namespace {
 
-constexpr int kGqaThreads = 6 * 32;
-constexpr int kTmaWarp = 4;
-constexpr int kIssueWarp = 5;
+constexpr int kGqaThreads = 10 * 32;
+constexpr int kTmaWarp = 8;
+constexpr int kIssueWarp = 9;
 constexpr int kQCols = 16;  // query heads per CTA (the N of both products)
 constexpr uint32_t kFull = 0xffffffffu;
 constexpr float kTau = 8.0f;  // conditional rescale threshold, log2 units
@@ -52,24 +55,25 @@ struct GqaCfg {
   static constexpr int kZeroBytes = (D == 64) ? 128 * 64 * 2 : 0;
   static constexpr int kQOff = kZeroOff + kZeroBytes;  // Q, 16 rows, K-major
   static constexpr int kQBytes = kQCols * D * 2;
-  static constexpr int kPOff = kQOff + kQBytes;  // two P^T buffers, 16 rows x 128 keys, K-major
+  static constexpr int kPOff = kQOff + kQBytes;  // P^T per warpgroup, 16 rows x 128 keys, K-major
   static constexpr int kPBytes = kQCols * 128 * 2;
-  static constexpr int kSOff = kPOff + 2 * kPBytes;  // S^T staged as fp32 [128 keys][17]
+  static constexpr int kSOff = kPOff + 2 * kPBytes;  // S^T per warpgroup, fp32 [128 keys][17]
   static constexpr int kSStride = 17;
-  static constexpr int kVecOff = kSOff + 128 * kSStride * 4;  // alpha, l, m per query
-  static constexpr int kBarOff = kVecOff + 3 * kQCols * 4;
+  static constexpr int kSBytes = 128 * kSStride * 4;
+  static constexpr int kVecOff = kSOff + 2 * kSBytes;  // per warpgroup: alpha, l, m per query
+  static constexpr int kBarOff = kVecOff + 2 * 3 * kQCols * 4;
   static constexpr int kSmemBytes = kBarOff + 256 + 1024;
 };
 
 enum GqaBar : int {
   kGFull = 0,    // + stage
   kGEmpty = 4,   // + stage
-  kGS = 8,       // + S buffer (2)
-  kGP = 10,      // + P buffer (2)
-  kGO = 12,      // an O^T product has completed
-  kGQ = 13,      // Q (and the zero block) staged
-  kGDone = 14,   // every product issued has completed
-  kGNumBars = 15,
+  kGS = 8,       // + warpgroup: its S^T is in TMEM
+  kGP = 10,      // + warpgroup: its P^T is in shared memory (and O^T rescaled)
+  kGO = 12,      // + warpgroup: its O^T product has completed
+  kGQ = 14,      // Q (and the zero block) staged
+  kGDone = 15,   // every product issued has completed
+  kGNumBars = 16,
 };
 
 struct GqaParams {
@@ -100,10 +104,6 @@ __global__ void __launch_bounds__(kGqaThreads, 1)
   uint8_t* base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint8_t* sq = base + C::kQOff;
   uint8_t* sp = base + C::kPOff;
-  float* sS = reinterpret_cast<float*>(base + C::kSOff);
-  float* s_alpha = reinterpret_cast<float*>(base + C::kVecOff);
-  float* s_l = s_alpha + kQCols;
-  float* s_m = s_l + kQCols;
   uint64_t* bars = reinterpret_cast<uint64_t*>(base + C::kBarOff);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(&bars[kGNumBars]);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(&bars[kGNumBars + 1]);
@@ -142,8 +142,8 @@ __global__ void __launch_bounds__(kGqaThreads, 1)
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars[kGS + i], 1);
       mbar_init(&bars[kGP + i], 1);
+      mbar_init(&bars[kGO + i], 1);
     }
-    mbar_init(&bars[kGO], 1);
     mbar_init(&bars[kGQ], 1);
     mbar_init(&bars[kGDone], 1);
     *abort_flag = 0;
@@ -157,7 +157,7 @@ __global__ void __launch_bounds__(kGqaThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  // TMEM columns: S^T buffers [0,16) and [16,32), O^T [32,48)
+  // TMEM columns: S^T of warpgroup w at [16w, 16w+16), its O^T at [32+16w, 48+16w)
   constexpr uint32_t kColO = 32;
 
   if (warp == kTmaWarp) {
@@ -192,13 +192,20 @@ __global__ void __launch_bounds__(kGqaThreads, 1)
       constexpr uint32_t idesc_o = idesc_bf16_f32(128, kQCols, true, false);
       bool ok = bounded_wait(&bars[kGQ], 0, abort_flag, p.err, kSiteQFull);
       const uint32_t q_addr = smem_u32(sq);
-      for (int t = 0; t <= n_tiles && ok; ++t) {
-        if (t < n_tiles) {
-          // S^T_t = K_t Q^T into S buffer t % 2
-          const int st = t % C::kStages;
-          if (!(ok = bounded_wait(&bars[kGFull + st], (t / C::kStages) & 1, abort_flag, p.err, kSiteKvFull))) break;
+      // Issue S_t as soon as tile t has landed (and its warpgroup's S buffer
+      // is free, i.e. O_{t-2} has been issued) and O_u as soon as P_u is
+      // written, whichever comes first: waiting for the next tile before the
+      // pending O product would hold its stage and starve the copies.
+      int next_s = 0, next_o = 0;
+      uint64_t idle_since = 0;
+      while (ok && next_o < n_tiles) {
+        bool progressed = false;
+        if (next_s < n_tiles && next_s - next_o <= 1 &&
+            mbar_try_wait(&bars[kGFull + next_s % C::kStages], (next_s / C::kStages) & 1)) {
+          // S^T_t = K_t Q^T into the S buffer of warpgroup t % 2
+          const int t = next_s;
           tc_fence_after();
-          const uint32_t k_addr = smem_u32(base + st * C::kStageBytes);
+          const uint32_t k_addr = smem_u32(base + (t % C::kStages) * C::kStageBytes);
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t ka = k_addr + static_cast<uint32_t>((kk / 4) * kChunkBytes + (kk % 4) * 32);
@@ -207,28 +214,43 @@ __global__ void __launch_bounds__(kGqaThreads, 1)
                     smem_desc_sw128(qa, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
           }
           umma_commit(&bars[kGS + (t & 1)]);
+          ++next_s;
+          progressed = true;
         }
-        if (t >= 1) {
-          // O^T += V_{t-1}^T P_{t-1}^T once the softmax has written P_{t-1}
-          const int u = t - 1;
+        if (next_o < next_s && mbar_try_wait(&bars[kGP + (next_o & 1)], (next_o >> 1) & 1)) {
+          // O^T of warpgroup u % 2 += V_u^T P_u^T
+          const int u = next_o, w = u & 1;
           const int st = u % C::kStages;
-          if (!(ok = bounded_wait(&bars[kGP + (u & 1)], (u >> 1) & 1, abort_flag, p.err, kSitePFull))) break;
           tc_fence_after();
           const uint32_t v_addr = smem_u32(base + st * C::kStageBytes + C::kTileBytes);
           // MN-major A: M = d in 64-element chunks; for d = 64 the second chunk
           // is the zero block (its distance from this stage's V tile)
           const uint32_t lbo =
               (D == 128) ? static_cast<uint32_t>(kChunkBytes) : smem_u32(base + C::kZeroOff) - v_addr;
-          const uint32_t p_addr = smem_u32(sp + (u & 1) * C::kPBytes);
+          const uint32_t p_addr = smem_u32(sp + w * C::kPBytes);
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk) {
             const uint32_t va = v_addr + static_cast<uint32_t>(kk * 2048);
             const uint32_t pa = p_addr + static_cast<uint32_t>((kk / 4) * (kQCols * 128) + (kk % 4) * 32);
-            umma_ss(tmem + kColO, smem_desc_sw128(va, lbo, 1024), smem_desc_sw128(pa, 16, 1024), idesc_o,
-                    (u > 0 || kk > 0) ? 1u : 0u);
+            umma_ss(tmem + kColO + static_cast<uint32_t>(w * kQCols), smem_desc_sw128(va, lbo, 1024),
+                    smem_desc_sw128(pa, 16, 1024), idesc_o, ((u >> 1) > 0 || kk > 0) ? 1u : 0u);
           }
           umma_commit(&bars[kGEmpty + st]);
-          umma_commit(&bars[kGO]);
+          umma_commit(&bars[kGO + w]);
+          ++next_o;
+          progressed = true;
+        }
+        // bounded: give up when nothing has been ready for the wait limit
+        if (progressed) {
+          idle_since = 0;
+        } else if (*abort_flag) {
+          ok = false;
+        } else if (idle_since == 0) {
+          idle_since = globaltimer_ns();
+        } else if (globaltimer_ns() - idle_since > kWaitTimeoutNs) {
+          *abort_flag = 1;
+          record_timeout(p.err, next_s < n_tiles ? kSiteKvFull : kSitePFull);
+          ok = false;
         }
       }
       // every product must complete before TMEM is freed
@@ -237,8 +259,15 @@ __global__ void __launch_bounds__(kGqaThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ softmax, rescale, epilogue
+    const int wg = warp >> 2;        // warpgroup: tiles wg, wg + 2, ...
+    const int wt = tid & 127;        // thread within the warpgroup
+    const int bar_id = 1 + wg;       // its named barrier
+    float* sS = reinterpret_cast<float*>(base + C::kSOff + wg * C::kSBytes);
+    float* s_alpha = reinterpret_cast<float*>(base + C::kVecOff) + wg * 3 * kQCols;
+    float* s_l = s_alpha + kQCols;
+    float* s_m = s_l + kQCols;
     // stage Q (rows >= nq are zero) and, for d = 64, the zero block
-    for (int i = tid; i < kQCols * (D / 8); i += 128) {
+    for (int i = tid; i < kQCols * (D / 8); i += 256) {
       const int r = i / (D / 8), u = i % (D / 8);  // row, 16-byte unit along d
       uint4 val = make_uint4(0, 0, 0, 0);
       if (r < nq)
@@ -247,36 +276,40 @@ __global__ void __launch_bounds__(kGqaThreads, 1)
       *reinterpret_cast<uint4*>(sq + (u / 8) * (kQCols * 128) + r * 128 + (((u % 8) ^ (r & 7)) << 4)) = val;
     }
     if constexpr (D == 64) {
-      for (int i = tid; i < C::kZeroBytes / 16; i += 128)
+      for (int i = tid; i < C::kZeroBytes / 16; i += 256)
         reinterpret_cast<uint4*>(base + C::kZeroOff)[i] = make_uint4(0, 0, 0, 0);
     }
     fence_proxy_async_smem();
-    named_bar_sync(1, 128);
+    named_bar_sync(3, 256);
     if (tid == 0) mbar_arrive(&bars[kGQ]);
 
-    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
-    const int qi = tid >> 3;   // query column of the transposed phase
-    const int seg = tid & 7;   // its 16 keys: seg*16 .. seg*16+15
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t s_col = static_cast<uint32_t>(wg * kQCols);
+    const uint32_t o_col = kColO + static_cast<uint32_t>(wg * kQCols);
+    const int qi = wt >> 3;   // query column of the transposed phase
+    const int seg = wt & 7;   // its 16 keys: seg*16 .. seg*16+15
     float m_run = -INFINITY, l_run = 0.f;
     bool ok = true;
-    for (int t = 0; t < n_tiles; ++t) {
+    int tiles_done = 0;
+    for (int t = wg; t < n_tiles; t += 2) {
+      const int j = t >> 1;  // this warpgroup's tile count so far
       const int st = t % C::kStages;
       const int valid = min(128, k_end - (k_begin + t * 128));  // keys of this tile inside the split
-      ok = bounded_wait(&bars[kGS + (t & 1)], (t >> 1) & 1, abort_flag, p.err, kSiteSFull);
-      if (!named_bar_and(1, 128, ok)) {
+      ok = bounded_wait(&bars[kGS + wg], j & 1, abort_flag, p.err, kSiteSFull);
+      if (!named_bar_and(bar_id, 128, ok)) {
         ok = false;
         break;
       }
       tc_fence_after();
       {
-        // S^T row of key `tid` -> shared memory [key][query]
+        // S^T row of key wt -> shared memory [key][query]
         uint32_t r[16];
-        tmem_ld_x16(tmem + lane_base + static_cast<uint32_t>((t & 1) * kQCols), r);
-        float* row = sS + tid * C::kSStride;
+        tmem_ld_x16(tmem + lane_base + s_col, r);
+        float* row = sS + wt * C::kSStride;
 #pragma unroll
-        for (int j = 0; j < kQCols; ++j) row[j] = __uint_as_float(r[j]);
+        for (int q = 0; q < kQCols; ++q) row[q] = __uint_as_float(r[q]);
       }
-      named_bar_sync(1, 128);
+      named_bar_sync(bar_id, 128);
       // 16 keys of query qi
       float x[16];
       float tmax = -INFINITY;
@@ -292,7 +325,7 @@ __global__ void __launch_bounds__(kGqaThreads, 1)
       float alpha = 1.f;
       bool rescale = false;
       if (m_run == -INFINITY) {
-        m_run = tmax;  // first tile: O^T is overwritten by its first product
+        m_run = tmax;  // first tile of this group: its O^T is overwritten by the product
       } else if (tmax - m_run > kTau) {
         alpha = ex2_approx(m_run - tmax);
         m_run = tmax;
@@ -311,7 +344,7 @@ __global__ void __launch_bounds__(kGqaThreads, 1)
       l_run = l_run * alpha + sum;
       // P^T row qi, keys seg*16..+15: two 16-byte units of chunk seg / 4
       {
-        uint8_t* prow = sp + (t & 1) * C::kPBytes + (seg / 4) * (kQCols * 128) + qi * 128;
+        uint8_t* prow = sp + wg * C::kPBytes + (seg / 4) * (kQCols * 128) + qi * 128;
         const int u0 = (seg % 4) * 2;
         *reinterpret_cast<uint4*>(prow + ((u0 ^ (qi & 7)) << 4)) = make_uint4(pw[0], pw[1], pw[2], pw[3]);
         *reinterpret_cast<uint4*>(prow + (((u0 + 1) ^ (qi & 7)) << 4)) = make_uint4(pw[4], pw[5], pw[6], pw[7]);
@@ -321,7 +354,7 @@ __global__ void __launch_bounds__(kGqaThreads, 1)
       // anything, NaN included): zero them in the V tile
       if (valid < 128) {
         uint8_t* vt = base + st * C::kStageBytes + C::kTileBytes;
-        for (int i = tid; i < (128 - valid) * C::kChunks * 8; i += 128) {
+        for (int i = wt; i < (128 - valid) * C::kChunks * 8; i += 128) {
           const int r = valid + i / (C::kChunks * 8);
           const int rem = i % (C::kChunks * 8);
           *reinterpret_cast<uint4*>(vt + (rem / 8) * kChunkBytes + r * 128 + (rem % 8) * 16) =
@@ -329,11 +362,11 @@ __global__ void __launch_bounds__(kGqaThreads, 1)
         }
       }
       fence_proxy_async_smem();
-      const bool any_rescale = named_bar_or(1, 128, rescale);
-      // the previous O^T product must be complete before O^T is touched again
-      if (t >= 1) {
-        ok = bounded_wait(&bars[kGO], (t - 1) & 1, abort_flag, p.err, kSiteOFull);
-        if (!named_bar_and(1, 128, ok)) {
+      const bool any_rescale = named_bar_or(bar_id, 128, rescale);
+      // this group's previous O^T product must be complete before O^T is touched again
+      if (j >= 1) {
+        ok = bounded_wait(&bars[kGO + wg], (j - 1) & 1, abort_flag, p.err, kSiteOFull);
+        if (!named_bar_and(bar_id, 128, ok)) {
           ok = false;
           break;
         }
@@ -341,32 +374,44 @@ __global__ void __launch_bounds__(kGqaThreads, 1)
       if (any_rescale) {
         tc_fence_after();
         uint32_t r[16];
-        tmem_ld_x16(tmem + lane_base + kColO, r);
+        tmem_ld_x16(tmem + lane_base + o_col, r);
 #pragma unroll
-        for (int j = 0; j < kQCols; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * s_alpha[j]);
-        tmem_st_x16(tmem + lane_base + kColO, r);
+        for (int q = 0; q < kQCols; ++q) r[q] = __float_as_uint(__uint_as_float(r[q]) * s_alpha[q]);
+        tmem_st_x16(tmem + lane_base + o_col, r);
         tmem_st_wait();
       }
       tc_fence_before();
-      named_bar_sync(1, 128);
-      if (tid == 0) mbar_arrive(&bars[kGP + (t & 1)]);
+      named_bar_sync(bar_id, 128);
+      if (wt == 0) mbar_arrive(&bars[kGP + wg]);
+      ++tiles_done;
     }
-    // epilogue: partials o / l and m + log2 l of every query of the group
-    if (ok) ok = bounded_wait(&bars[kGO], (n_tiles - 1) & 1, abort_flag, p.err, kSiteOFull);
+    // this group's last product, then its summary (m, l) per query
+    if (ok && tiles_done > 0) ok = bounded_wait(&bars[kGO + wg], (tiles_done - 1) & 1, abort_flag, p.err, kSiteOFull);
     if (seg == 0) {
       s_l[qi] = l_run;
       s_m[qi] = m_run;
     }
-    if (named_bar_and(1, 128, ok)) {
+    // epilogue by warpgroup 0: merge the two groups' (m, l, O^T) (combine
+    // operator), then the partials o / l and m + log2 l of every query
+    if (named_bar_and(3, 256, ok) && wg == 0) {
       tc_fence_after();
-      uint32_t r[16];
-      tmem_ld_x16(tmem + lane_base + kColO, r);
-      if (tid < D) {
+      const float* l1 = s_l + 3 * kQCols;  // warpgroup 1's vectors
+      const float* m1 = s_m + 3 * kQCols;
+      uint32_t r0[16], r1[16];
+      tmem_ld_x16(tmem + lane_base + kColO, r0);
+      tmem_ld_x16(tmem + lane_base + kColO + kQCols, r1);
+      if (wt < D) {
         for (int q = 0; q < nq; ++q) {
           const size_t idx = (static_cast<size_t>(b) * p.Hq + hq0 + q) * p.S + s;
-          const float l = s_l[q];
-          p.ws_o[idx * D + tid] = (l > 0.f) ? __uint_as_float(r[q]) / l : 0.f;
-          if (tid == 0) p.ws_lse[idx] = (l > 0.f) ? s_m[q] + log2f(l) : -INFINITY;
+          const float ma = s_m[q], mb = m1[q];
+          const float mx = fmaxf(ma, mb);  // finite: group 0 saw at least one key
+          const float wa = ex2_approx(ma - mx);
+          const float wb = (mb == -INFINITY) ? 0.f : ex2_approx(mb - mx);
+          const float l = wa * s_l[q] + wb * l1[q];
+          // group 1's accumulator is never written when it saw no tile
+          const float acc = wa * __uint_as_float(r0[q]) + ((wb > 0.f) ? wb * __uint_as_float(r1[q]) : 0.f);
+          p.ws_o[idx * D + wt] = (l > 0.f) ? acc / l : 0.f;
+          if (wt == 0) p.ws_lse[idx] = (l > 0.f) ? mx + log2f(l) : -INFINITY;
         }
       }
     }
