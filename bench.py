@@ -35,6 +35,8 @@ METRIC = "attn fwd TFLOP/s (% of GB300 BF16 peak); decode KV-read GB/s (% of HBM
 PREFILL_NAME = "llama3_8b_prefill"
 DECODE_NAME = "decode_32k"
 DEFAULT_SPLITS = 16
+GQA_NAME = "decode_gqa8_32k"
+GQA_SPLITS = 8
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 FALLBACK_BF16_TFLOPS_SUSTAINED = 1700.0
@@ -325,6 +327,28 @@ def run_gpu(args, world, rank, local):
     bwd_flops = perfmodel.bwd_flops(pc.B, pc.H, pc.N, pc.d, pc.causal)
     bwd_value = world * bwd_flops * bwd_steps / (bwd_ms * 1e-3) / 1e12
 
+    # GQA decode (64 query heads over 8 K/V heads), timed on its own after the step loop
+    gc = wl.DECODE_GQA[GQA_NAME]
+    gq, gkc, gvc, gsl = wl.decode_gqa_inputs(gc.B, gc.Hq, gc.Hkv, gc.L, gc.d, seed=rank, device=dev)
+    go = torch.empty_like(gq)
+    glse = torch.empty((gc.B, gc.Hq), dtype=torch.float32, device=dev)
+    for _ in range(3):
+        fa.fa_decode_gqa(gq, gkc, gvc, gsl, GQA_SPLITS, o=go, lse=glse, stream=stream)
+    torch.cuda.synchronize(dev)
+    g0 = torch.cuda.Event(enable_timing=True)
+    g1 = torch.cuda.Event(enable_timing=True)
+    gqa_steps = max(1, min(args.steps, 50))
+    g0.record(stream)
+    for _ in range(gqa_steps):
+        fa.fa_decode_gqa(gq, gkc, gvc, gsl, GQA_SPLITS, o=go, lse=glse, stream=stream)
+    g1.record(stream)
+    torch.cuda.synchronize(dev)
+    fa.fa_check_device_error(stream)
+    gqa_ms = reduce_max([g0.elapsed_time(g1)], world)[0]
+    gqa_kv = perfmodel.decode_kv_bytes(gc.Hkv, gc.d, gsl.tolist())
+    gqa_gbs = world * gqa_kv * gqa_steps / (gqa_ms * 1e-3) / 1e9
+    del gkc, gvc
+
     # end to end through the public API with pinned host buffers: H2D of q/k/v,
     # the C-ABI call, D2H of o and lse, all inside the timed region
     hq, hk, hv = (t.cpu().pin_memory() for t in (q, k, v))
@@ -386,6 +410,10 @@ def run_gpu(args, world, rank, local):
         "decode": {"value": dec_gbs, "unit": "GB/s (KV read)", "frac_of_hbm": dec_gbs / peaks["hbm_gbs"],
                    "ms_per_step": dec_avg_ms},
         "prefill_ms_per_step": fwd_avg_ms,
+        "decode_gqa": {"value": gqa_gbs, "unit": "GB/s (KV read)", "ms_per_call": gqa_ms / gqa_steps,
+                       "steps": gqa_steps, "frac_of_hbm": gqa_gbs / peaks["hbm_gbs"],
+                       "what": f"fa_decode_gqa on {GQA_NAME} (B{gc.B} Hq{gc.Hq} Hkv{gc.Hkv} L{gc.L} d{gc.d}), "
+                               f"{GQA_SPLITS} splits, timed after the step loop"},
         "backward": {"value": bwd_value, "unit": "TFLOP/s (10 N^2 d per head, halved causal)",
                      "ms_per_call": bwd_ms / bwd_steps, "steps": bwd_steps,
                      "frac_of_bf16_peak": bwd_value / world / peaks["bf16_tflops"],
