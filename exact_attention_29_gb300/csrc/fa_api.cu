@@ -103,10 +103,11 @@ unsigned int* device_error_word() {
 
 namespace {
 
-// A 3-D map over [outer][rows][d] with 128-byte swizzle and a box of
-// box_inner x box_rows x 1 elements (box_inner x elem_bytes = 128 bytes).
-bool encode_3d(CUtensorMap* map, CUtensorMapDataType dtype, uint64_t elem_bytes, uint32_t box_inner, const void* base,
-               uint64_t d, uint64_t rows, uint64_t outer, uint32_t box_rows) {
+// A 3-D map over [outer][rows][inner] with 128-byte swizzle, rows row_pitch
+// bytes apart, and a box of box_inner x box_rows x 1 elements
+// (box_inner x elem_bytes = 128 bytes).
+bool encode_3d(CUtensorMap* map, CUtensorMapDataType dtype, uint32_t box_inner, const void* base, uint64_t inner,
+               uint64_t rows, uint64_t outer, uint32_t box_rows, uint64_t row_pitch) {
   {
     std::lock_guard<std::mutex> lock(g_mutex);
     if (g_encode == nullptr) {
@@ -121,8 +122,8 @@ bool encode_3d(CUtensorMap* map, CUtensorMapDataType dtype, uint64_t elem_bytes,
       g_encode = reinterpret_cast<EncodeTiledFn>(fn);
     }
   }
-  const cuuint64_t dims[3] = {d, rows, outer};
-  const cuuint64_t strides[2] = {d * elem_bytes, rows * d * elem_bytes};
+  const cuuint64_t dims[3] = {inner, rows, outer};
+  const cuuint64_t strides[2] = {row_pitch, rows * row_pitch};
   const cuuint32_t box[3] = {box_inner, box_rows, 1};
   const cuuint32_t estr[3] = {1, 1, 1};
   const CUresult r = g_encode(map, dtype, 3, const_cast<void*>(base), dims, strides, box, estr,
@@ -141,12 +142,17 @@ bool encode_3d(CUtensorMap* map, CUtensorMapDataType dtype, uint64_t elem_bytes,
 
 bool encode_bf16_map(CUtensorMap* map, const void* base, uint64_t d, uint64_t rows, uint64_t outer,
                      uint32_t box_rows) {
-  return encode_3d(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 64, base, d, rows, outer, box_rows);
+  return encode_3d(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 64, base, d, rows, outer, box_rows, d * 2);
+}
+
+bool encode_u8_map(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint64_t outer,
+                   uint32_t box_rows, uint64_t row_pitch) {
+  return encode_3d(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 128, base, inner, rows, outer, box_rows, row_pitch);
 }
 
 bool encode_f32_map(CUtensorMap* map, const void* base, uint64_t d, uint64_t rows, uint64_t outer,
                     uint32_t box_rows) {
-  return encode_3d(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, 32, base, d, rows, outer, box_rows);
+  return encode_3d(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 32, base, d, rows, outer, box_rows, d * 4);
 }
 
 }  // namespace fa
@@ -340,7 +346,7 @@ fa_status fa_fwd_plan(int N, int block, int causal, long long* pairs_total, long
 
 fa_status fa_selftest_mma(int mode, const void* a, const void* b, float* d, int n, int k, fa_stream_t stream) {
   if (!a || !b || !d || !aligned16(a) || !aligned16(b) || !aligned4(d)) return FA_ERR_INVALID_ARG;
-  if (mode != 0 && mode != 1) return FA_ERR_INVALID_ARG;
+  if (mode < 0 || mode > 3) return FA_ERR_INVALID_ARG;
   int dev = -1;
   fa_status st = current_device(&dev);
   if (st != FA_OK) return st;

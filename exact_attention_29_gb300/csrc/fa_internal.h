@@ -14,6 +14,10 @@ namespace fa {
 // box and 128-byte swizzle. Returns false (and sets the error text) on failure.
 bool encode_bf16_map(CUtensorMap* map, const void* base, uint64_t d, uint64_t rows, uint64_t outer,
                      uint32_t box_rows);
+// A 3-D uint8 (e4m3 codes) map over [outer][rows][inner], rows row_pitch bytes
+// apart (a multiple of 16), {128, box_rows, 1} box, 128-byte swizzle.
+bool encode_u8_map(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint64_t outer,
+                   uint32_t box_rows, uint64_t row_pitch);
 // The same over fp32 elements with a {32, box_rows, 1} box (128-byte rows).
 bool encode_f32_map(CUtensorMap* map, const void* base, uint64_t d, uint64_t rows, uint64_t outer,
                     uint32_t box_rows);

@@ -61,4 +61,30 @@ __device__ __forceinline__ void issue_mn_mn(uint32_t d_tmem, uint32_t a_smem, ui
   }
 }
 
+// FP8 (e4m3) forms of the two products for d = 128: every 128-row tile row is
+// 128 bytes, one swizzle chunk; one instruction covers K = 32 (32 bytes).
+// S(tmem, 128 x 128 fp32) = Q(smem, 128 x 128 e4m3, K-major) * K(smem, 128 x 128 e4m3, K-major)^T
+__device__ __forceinline__ void issue_qk_f8(uint32_t s_tmem, uint32_t q_smem, uint32_t k_smem) {
+  constexpr uint32_t idesc = idesc_e4m3_f32(kBM, kBN);
+#pragma unroll
+  for (int kk = 0; kk < 4; ++kk) {
+    const uint32_t off = static_cast<uint32_t>(kk * 32);
+    umma_ss_f8(s_tmem, smem_desc_sw128(q_smem + off, 16, 1024), smem_desc_sw128(k_smem + off, 16, 1024), idesc,
+               kk > 0 ? 1u : 0u);
+  }
+}
+
+// O(tmem, 128 x 128 fp32) (+)= P(tmem, 128 x 128 e4m3, four keys per column) * V,
+// V given as V^T (smem, 128 rows of d x 128 keys e4m3, K-major). Keys 32kk..32kk+31
+// of P sit in TMEM columns [p + 8kk, p + 8kk + 8).
+__device__ __forceinline__ void issue_pv_f8(uint32_t o_tmem, uint32_t p_tmem, uint32_t vt_smem, bool accumulate) {
+  constexpr uint32_t idesc = idesc_e4m3_f32(kBM, 128);
+#pragma unroll
+  for (int kk = 0; kk < 4; ++kk) {
+    umma_ts_f8(o_tmem, p_tmem + static_cast<uint32_t>(kk * 8),
+               smem_desc_sw128(vt_smem + static_cast<uint32_t>(kk * 32), 16, 1024), idesc,
+               (accumulate || kk > 0) ? 1u : 0u);
+  }
+}
+
 }  // namespace fa

@@ -2,7 +2,7 @@
 // through the C ABI so the test suite can check each one on the GPU alone:
 //   * one tensor-core product through the same TMA staging, shared-memory
 //     descriptors and TMEM placement as the prefill kernel (issue_qk and
-//     issue_pv from fa_mma.cuh);
+//     issue_pv from fa_mma.cuh, bf16; issue_qk_f8 and issue_pv_f8, e4m3);
 //   * the bounded-wait path: a wait on a barrier nothing arrives at must give
 //     up, record the timeout and return.
 #include <cuda_bf16.h>
@@ -101,6 +101,101 @@ __global__ void __launch_bounds__(128, 1)
   }
 }
 
+// e4m3 products, 128 x 128 x 128:
+//   mode 2: D = A B^T, A [128][128] and B [128][128] e4m3 K-major (issue_qk_f8)
+//   mode 3: D = A B^T with A placed in TMEM (four e4m3 per column) and B
+//           [128][128] K-major in shared memory (issue_pv_f8, B = V^T)
+__global__ void __launch_bounds__(128, 1)
+    mma_f8_test_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
+                       const uint8_t* __restrict__ a_gmem, float* __restrict__ d, int mode, unsigned int* err) {
+  extern __shared__ uint8_t raw[];
+  uint8_t* base = raw + ((1024u - (smem_u32(raw) & 1023u)) & 1023u);
+  constexpr int kT = 128 * 128;
+  uint8_t* sa = base;
+  uint8_t* sb = base + kT;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(base + 2 * kT);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    mbar_init(&bars[0], 1);
+    mbar_init(&bars[1], 1);
+    fence_barrier_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(tmem_slot, 256);  // D in [0, 128), A (mode 3) in [128, 160)
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+  if (mode == 3) {
+    const uint32_t* arow = reinterpret_cast<const uint32_t*>(a_gmem + static_cast<size_t>(threadIdx.x) * 128);
+    uint32_t r[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) r[i] = arow[i];
+    tmem_st_x32(tmem + lane_base + 128, r);
+    tmem_st_wait();
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    tc_fence_after();
+    mbar_arrive_expect_tx(&bars[0], mode == 2 ? 2 * kT : kT);
+    if (mode == 2) tma_load_3d(sa, &tm_a, &bars[0], 0, 0, 0);
+    tma_load_3d(sb, &tm_b, &bars[0], 0, 0, 0);
+    const bool ok = bounded_wait(&bars[0], 0, nullptr, err, kSiteSelftest);
+    if (ok) {
+      tc_fence_after();
+      if (mode == 2)
+        issue_qk_f8(tmem, smem_u32(sa), smem_u32(sb));
+      else
+        issue_pv_f8(tmem, tmem + 128, smem_u32(sb), false);
+    }
+    umma_commit(&bars[1]);
+  }
+  __syncwarp();
+  const bool done = bounded_wait(&bars[1], 0, nullptr, err, kSiteSelftest);
+  if (__all_sync(0xffffffffu, done)) {
+    tc_fence_after();
+    const int row = warp * 32 + lane;
+#pragma unroll 1
+    for (int c = 0; c < 128; c += 32) {
+      uint32_t r[32];
+      tmem_ld_x32(tmem + lane_base + c, r);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) d[static_cast<size_t>(row) * 128 + c + i] = __uint_as_float(r[i]);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, 256);
+  }
+}
+
+fa_status launch_mma_f8(int mode, const void* a, const void* b, float* d, cudaStream_t stream, unsigned int* err) {
+  CUtensorMap ta, tb;
+  if (!encode_u8_map(&ta, a, 128, 128, 1, 128, 128) || !encode_u8_map(&tb, b, 128, 128, 1, 128, 128))
+    return FA_ERR_CUDA;
+  constexpr int smem = 2 * 128 * 128 + 64 + 1024;
+  cudaError_t e = cudaFuncSetAttribute(mma_f8_test_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) {
+    set_error_text("cudaFuncSetAttribute(mma_f8_test_kernel)", e);
+    return FA_ERR_CUDA;
+  }
+  mma_f8_test_kernel<<<1, 128, smem, stream>>>(ta, tb, static_cast<const uint8_t*>(a), d, mode, err);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) {
+    set_error_text("mma_f8_test_kernel launch", e);
+    return FA_ERR_CUDA;
+  }
+  return FA_OK;
+}
+
 __global__ void wait_test_kernel(unsigned int* err, unsigned long long timeout_ns) {
   __shared__ uint64_t bar;
   if (threadIdx.x == 0) {
@@ -145,6 +240,7 @@ fa_status launch_selftest_mma(int mode, const void* a, const void* b, float* d, 
   if (mode == 0 && n == 128 && k == 64) return launch_mma<64, 128>(0, a, b, d, stream, err);
   if (mode == 1 && n == 128 && k == 128) return launch_mma<128, 128>(1, a, b, d, stream, err);
   if (mode == 1 && n == 64 && k == 128) return launch_mma<128, 64>(1, a, b, d, stream, err);
+  if ((mode == 2 || mode == 3) && n == 128 && k == 128) return launch_mma_f8(mode, a, b, d, stream, err);
   return FA_ERR_UNSUPPORTED;
 }
 

@@ -211,7 +211,12 @@ fa_status fa_fwd_plan(int N, int block, int causal, long long *pairs_total, long
  *   mode 1: D[128][n] = A[128][k] * B[k][n], A placed in tensor memory as packed
  *           bf16 pairs, B MN-major in shared memory (the O += P V product),
  *           k = 128, n in {64, 128}.
- *   a, b: bf16 device pointers; d: fp32 device pointer [128][n].
+ *   mode 2: as mode 0 with e4m3 A and B (kind::f8f6f4), n = k = 128.
+ *   mode 3: D = A * B^T with A placed in tensor memory as four e4m3 per 32-bit
+ *           column and B [n][k] K-major in shared memory (the O += P V product
+ *           with V given transposed), n = k = 128.
+ *   a, b: bf16 (modes 0, 1) or e4m3 byte (modes 2, 3) device pointers;
+ *   d: fp32 device pointer [128][n].
  *
  * fa_selftest_wait_timeout: launch one block that waits on a barrier nothing
  *   ever arrives at, bounded by `timeout_us`; the kernel gives up, records

@@ -44,6 +44,29 @@ def test_mma_pv_tmem_a_mn_major_b(n):
     assert err <= 1e-3, err
 
 
+def _rand_e4m3(shape, seed):
+    """e4m3 codes (uint8) and their values, from torch's float8_e4m3fn."""
+    g = torch.Generator().manual_seed(seed)
+    x = (torch.randn(shape, generator=g) * 8).to(torch.float8_e4m3fn)
+    return x.view(torch.uint8), x.float().double()
+
+
+@pytest.mark.parametrize("mode", [2, 3])
+def test_mma_e4m3(mode):
+    """D = A B^T with e4m3 operands (kind::f8f6f4): mode 2 both K-major in shared
+    memory (S = Q K^T), mode 3 A in tensor memory, four values per column, and B
+    K-major in shared memory (O += P V with V transposed)."""
+    import exact_attention_29_gb300 as fa
+
+    (a, av), (b, bv) = _rand_e4m3((128, 128), 5 + mode), _rand_e4m3((128, 128), 7 + mode)
+    d = fa.fa_selftest_mma(mode, a.cuda(), b.cuda(), 128, 128)
+    fa.fa_check_device_error()
+    ref = av @ bv.T
+    err = (d.double().cpu() - ref).abs().max().item()
+    # products of e4m3 values are exact in fp32; 128-term fp32 sums of |terms| <= 448^2
+    assert err <= 1e-6 * ref.abs().max().item() + 1e-3, err
+
+
 def test_bounded_wait_times_out_and_context_survives():
     """A wait on a barrier nothing arrives at gives up after its limit, the host
     reads FA_ERR_TIMEOUT, the word is cleared, and the GPU keeps working."""
