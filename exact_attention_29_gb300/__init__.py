@@ -20,6 +20,8 @@ from ._lib import (  # noqa: F401
     fa_decode_gqa,
     fa_decode_noalloc,
     fa_fwd,
+    fa_fwd_fp8,
+    fa_quantize_fp8,
     fa_fwd_plan,
     fa_selftest_mma,
     fa_selftest_wait_timeout,

@@ -33,6 +33,8 @@ _SIGNATURES = {
     "fa_decode": ([_VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _VP], _I),
     "fa_bwd": ([_VP] * 9 + [_I] * 5 + [ctypes.c_float, _VP], _I),
     "fa_decode_gqa": ([_VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _I, _VP], _I),
+    "fa_quantize_fp8": ([_VP, _VP, _VP, _VP] + [_I] * 7 + [_VP], _I),
+    "fa_fwd_fp8": ([_VP] * 8 + [_I] * 5 + [ctypes.c_float, _I, _VP], _I),
     "fa_bwd_plan": ([_I, _I, _I, _I, ctypes.POINTER(ctypes.c_longlong)], _I),
     "fa_decode_noalloc": ([_VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _VP], _I),
     "fa_status_string": ([_I], ctypes.c_char_p),
@@ -120,6 +122,63 @@ def fa_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = Fal
     st = lib.fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), B, H, N, d,
                     1 if causal else 0, float(scale), _stream_handle(stream))
     _check(st, "fa_fwd")
+    return o, lse
+
+
+def _pitch16(n: int) -> int:
+    return (n + 15) // 16 * 16
+
+
+def fa_quantize_fp8(x: torch.Tensor, signs: torch.Tensor | None = None, per_head: bool = False,
+                    transpose: bool = False, stream=None):
+    """Block-quantize bf16 x [B, H, N, 128] to e4m3 codes (uint8).
+
+    signs: fp32 [128] of +-1 for the incoherent rotation (None: no rotation).
+    Returns (codes, scales): codes [B, H, N, 128] or, transposed, [B, H, 128,
+    pitch] with pitch = N rounded up to 16; scales [B, H, ceil(N/128)] or
+    [B, H] (per_head).
+    """
+    lib = load_library()
+    _require(x, "x", torch.bfloat16, 4)
+    B, H, N, d = x.shape
+    pitch = _pitch16(N)
+    if transpose:
+        codes = torch.zeros((B, H, d, pitch), dtype=torch.uint8, device=x.device)
+    else:
+        codes = torch.empty((B, H, N, d), dtype=torch.uint8, device=x.device)
+    tiles = (N + 127) // 128
+    scales = torch.empty((B, H) if per_head else (B, H, tiles), dtype=torch.float32, device=x.device)
+    sp = 0
+    if signs is not None:
+        _require(signs, "signs", torch.float32, 1)
+        sp = signs.data_ptr()
+    st = lib.fa_quantize_fp8(x.data_ptr(), sp, codes.data_ptr(), scales.data_ptr(), B, H, N, d, int(per_head),
+                             int(transpose), pitch if transpose else 0, _stream_handle(stream))
+    _check(st, "fa_quantize_fp8")
+    return codes, scales
+
+
+def fa_fwd_fp8(q8: torch.Tensor, k8: torch.Tensor, vt8: torch.Tensor, q_scale: torch.Tensor, k_scale: torch.Tensor,
+               v_scale: torch.Tensor, causal: bool = False, scale: float | None = None, o=None, lse=None,
+               stream=None):
+    """FP8 forward. q8, k8 uint8 [B, H, N, 128]; vt8 uint8 [B, H, 128, pitch];
+    scales from fa_quantize_fp8. Returns (o bf16 [B, H, N, 128], lse fp32 [B, H, N])."""
+    lib = load_library()
+    for t, n in ((q8, "q8"), (k8, "k8"), (vt8, "vt8")):
+        _require(t, n, torch.uint8, 4)
+    B, H, N, d = q8.shape
+    if k8.shape != q8.shape or vt8.shape[:3] != (B, H, d) or vt8.shape[3] < N:
+        raise ValueError("shapes must be q8, k8 [B,H,N,d] and vt8 [B,H,d,pitch >= N]")
+    if scale is None:
+        scale = d ** -0.5
+    if o is None:
+        o = torch.empty((B, H, N, d), dtype=torch.bfloat16, device=q8.device)
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q8.device)
+    st = lib.fa_fwd_fp8(q8.data_ptr(), k8.data_ptr(), vt8.data_ptr(), q_scale.data_ptr(), k_scale.data_ptr(),
+                        v_scale.data_ptr(), o.data_ptr(), lse.data_ptr(), B, H, N, d, 1 if causal else 0,
+                        float(scale), vt8.shape[3], _stream_handle(stream))
+    _check(st, "fa_fwd_fp8")
     return o, lse
 
 

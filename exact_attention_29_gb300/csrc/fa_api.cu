@@ -194,6 +194,61 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
                     g_num_sms[dev]);
 }
 
+fa_status fa_quantize_fp8(const void* x, const float* signs, void* codes, float* scales, int B, int H, int N, int d,
+                          int per_head, int transpose, int v_pitch, fa_stream_t stream) {
+  if (!x || !codes || !scales) return FA_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(codes) || !aligned4(scales) || (signs && !aligned4(signs))) return FA_ERR_INVALID_ARG;
+  if (B < 1 || H < 1 || N < 1 || d < 1) return FA_ERR_INVALID_ARG;
+  if ((per_head != 0 && per_head != 1) || (transpose != 0 && transpose != 1)) return FA_ERR_INVALID_ARG;
+  if (transpose && (v_pitch < N || v_pitch % 16 != 0)) return FA_ERR_INVALID_ARG;
+  if (d != 128) return FA_ERR_UNSUPPORTED;
+  const long long bh = static_cast<long long>(B) * H;
+  const long long tiles = (static_cast<long long>(N) + 127) / 128;
+  if (bh > 65535 || tiles > 0x7fffffffLL) return FA_ERR_INVALID_ARG;
+  int dev = -1;
+  fa_status st = current_device(&dev);
+  if (st != FA_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  void* ws = nullptr;
+  cudaError_t e = cudaMallocAsync(&ws, static_cast<size_t>(bh * tiles) * sizeof(float), s);
+  if (e != cudaSuccess) {
+    set_error_text("cudaMallocAsync(quantize workspace)", e);
+    return FA_ERR_CUDA;
+  }
+  st = launch_quantize_fp8(x, signs, codes, scales, B, H, N, per_head, transpose, transpose ? v_pitch : 0,
+                           static_cast<float*>(ws), s);
+  e = cudaFreeAsync(ws, s);
+  if (st == FA_OK && e != cudaSuccess) {
+    set_error_text("cudaFreeAsync(quantize workspace)", e);
+    st = FA_ERR_CUDA;
+  }
+  return st;
+}
+
+fa_status fa_fwd_fp8(const void* q8, const void* k8, const void* vt8, const float* q_scale, const float* k_scale,
+                     const float* v_scale, void* o, float* lse, int B, int H, int N, int d, int causal, float scale,
+                     int v_pitch, fa_stream_t stream) {
+  if (!q8 || !k8 || !vt8 || !q_scale || !k_scale || !v_scale || !o || !lse) return FA_ERR_INVALID_ARG;
+  if (!aligned16(q8) || !aligned16(k8) || !aligned16(vt8) || !aligned16(o) || !aligned4(lse) || !aligned4(q_scale) ||
+      !aligned4(k_scale) || !aligned4(v_scale))
+    return FA_ERR_INVALID_ARG;
+  if (B < 1 || H < 1 || N < 1 || d < 1) return FA_ERR_INVALID_ARG;
+  if (!(scale > 0.f) || !std::isfinite(scale)) return FA_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
+  if (v_pitch < N || v_pitch % 16 != 0) return FA_ERR_INVALID_ARG;
+  if (d != 128) return FA_ERR_UNSUPPORTED;
+  const long long bh = static_cast<long long>(B) * H;
+  const long long pairs = (static_cast<long long>(N) + 255) / 256;
+  if (bh > 0x7fffffffLL || pairs > 65535) return FA_ERR_INVALID_ARG;
+  int dev = -1;
+  fa_status st = current_device(&dev);
+  if (st != FA_OK) return st;
+  unsigned int* err = device_error_word();
+  if (!err) return FA_ERR_CUDA;
+  return launch_fwd_fp8(q8, k8, vt8, q_scale, k_scale, v_scale, o, lse, B, H, N, d, causal, scale, v_pitch,
+                        reinterpret_cast<cudaStream_t>(stream), err, g_num_sms[dev]);
+}
+
 fa_status fa_decode(const void* q, const void* k_cache, const void* v_cache, const int32_t* seqlens, void* o,
                     float* lse, int B, int H, int L, int d, int num_splits, fa_stream_t stream) {
   if (!q || !k_cache || !v_cache || !seqlens || !o || !lse) return FA_ERR_INVALID_ARG;

@@ -30,6 +30,13 @@
 //   TMEM A operand of O += P V. While warpgroup 0 runs the softmax of S0 the
 //   tensor core works on tile 1's products, and the other way round.
 //
+// The same kernel runs the FP8 path ("已有的几种大模型上下文支持情况" §4.4,
+// FA-3): e4m3 Q and K with one scale per 128-row tile (the product of the two
+// tile scales joins the softmax scale of each S tile), V given transposed as
+// e4m3 with one scale per head (applied with the final 1 / l), both products
+// on kind::f8f6f4, and P rounded to e4m3 (four keys per TMEM column) for the
+// P V product while l sums the fp32 values.
+//
 // Every role walks the same item sequence and keeps its own barrier phase
 // counters. Every wait is bounded (fa_common.cuh); a wait that runs out
 // records the site, raises the CTA abort flag, and every role drains its
@@ -53,11 +60,13 @@ constexpr float kRescaleSlack = 8.0f;  // log2 units: rescale only when the max 
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr uint32_t kFull = 0xffffffffu;
 
-template <int D>
+// F8: e4m3 Q, K and V^T (d = 128 only: a 128-byte row is one swizzle chunk).
+template <int D, bool F8 = false>
 struct Cfg {
-  static constexpr int kTileBytes = kBN * D * 2;  // one Q, K or V tile
-  static constexpr int kChunks = D / 64;
-  static constexpr int kStages = (D == 128) ? 4 : 8;  // K/V ring slots
+  static_assert(!F8 || D == 128, "e4m3 tiles need 128-byte rows");
+  static constexpr int kTileBytes = kBN * D * (F8 ? 1 : 2);  // one Q, K or V tile
+  static constexpr int kChunks = F8 ? 1 : D / 64;
+  static constexpr int kStages = (D == 128 && !F8) ? 4 : 8;  // K/V ring slots
   // TMEM column of S (and P) and of O for Q tile t
   __host__ __device__ static constexpr uint32_t s_col(int t) { return t ? 128u : 0u; }
   __host__ __device__ static constexpr uint32_t o_col(int t) { return t ? 256u + D : 256u; }
@@ -73,6 +82,11 @@ struct FwdParams {
   __nv_bfloat16* o;
   float* lse;
   unsigned int* err;
+  // e4m3 inputs only: per-tile scales of Q and K ([BH][tiles]) and per-head scale of V ([BH])
+  const float* sq;
+  const float* sk;
+  const float* sv;
+  int tiles;
   int N;
   int BH;          // batch * heads
   int num_pairs;   // Q-tile pairs per head
@@ -97,9 +111,9 @@ struct Smem {
   volatile int* abort_flag;
 };
 
-template <int D>
+template <int D, bool F8>
 __device__ __forceinline__ Smem carve(uint8_t* raw) {
-  using C = Cfg<D>;
+  using C = Cfg<D, F8>;
   const uint32_t a = smem_u32(raw);
   uint8_t* base = raw + ((1024u - (a & 1023u)) & 1023u);
   Smem s;
@@ -147,10 +161,10 @@ __device__ __forceinline__ bool item_at(const FwdParams& p, int k, Item& it) {
 }
 
 // ---------------------------------------------------------------- TMA producer (one thread)
-template <int D>
+template <int D, bool F8>
 __device__ void load_role(const CUtensorMap* tm_q, const CUtensorMap* tm_k, const CUtensorMap* tm_v, const Smem& sm,
                           const FwdParams& p) {
-  using C = Cfg<D>;
+  using C = Cfg<D, F8>;
   tma_prefetch_desc(tm_q);
   tma_prefetch_desc(tm_k);
   tma_prefetch_desc(tm_v);
@@ -183,9 +197,14 @@ __device__ void load_role(const CUtensorMap* tm_q, const CUtensorMap* tm_k, cons
         uint8_t* dst = sm.ring + slot * C::kTileBytes;
         mbar_arrive_expect_tx(&sm.kv_full[slot], C::kTileBytes);
         const CUtensorMap* map = kind ? tm_v : tm_k;
+        if (F8 && kind) {
+          // V^T: rows are d, the 128 keys of tile j are the inner coordinate
+          tma_load_3d(dst, map, &sm.kv_full[slot], j * kBN, 0, it.bh);
+        } else {
 #pragma unroll
-        for (int c = 0; c < C::kChunks; ++c)
-          tma_load_3d(dst + c * kChunkBytes, map, &sm.kv_full[slot], c * 64, j * kBN, it.bh);
+          for (int c = 0; c < C::kChunks; ++c)
+            tma_load_3d(dst + c * kChunkBytes, map, &sm.kv_full[slot], c * 64, j * kBN, it.bh);
+        }
         ++ring;
       }
     }
@@ -198,9 +217,25 @@ __device__ void load_role(const CUtensorMap* tm_q, const CUtensorMap* tm_k, cons
 }
 
 // ---------------------------------------------------------------- MMA issuer (one thread)
-template <int D>
+template <int D, bool F8>
+__device__ __forceinline__ void qk_product(uint32_t s_tmem, uint32_t q_smem, uint32_t k_smem) {
+  if constexpr (F8)
+    issue_qk_f8(s_tmem, q_smem, k_smem);
+  else
+    issue_qk<D>(s_tmem, q_smem, k_smem);
+}
+
+template <int D, bool F8>
+__device__ __forceinline__ void pv_product(uint32_t o_tmem, uint32_t p_tmem, uint32_t v_smem, bool accumulate) {
+  if constexpr (F8)
+    issue_pv_f8(o_tmem, p_tmem, v_smem, accumulate);
+  else
+    issue_pv<D>(o_tmem, p_tmem, v_smem, accumulate);
+}
+
+template <int D, bool F8>
 __device__ void mma_role(const Smem& sm, uint32_t tmem, const FwdParams& p) {
-  using C = Cfg<D>;
+  using C = Cfg<D, F8>;
   const uint32_t ring_base = smem_u32(sm.ring);
   const uint32_t qa0 = smem_u32(sm.q[0]);
   const uint32_t qa1 = smem_u32(sm.q[1]);
@@ -228,7 +263,7 @@ __device__ void mma_role(const Smem& sm, uint32_t tmem, const FwdParams& p) {
     tc_fence_after();
     for (int t = 0; t < 2; ++t) {
       if (it.n(t) == 0) continue;
-      issue_qk<D>(tmem + C::s_col(t), t ? qa1 : qa0, slot_addr(base));
+      qk_product<D, F8>(tmem + C::s_col(t), t ? qa1 : qa0, slot_addr(base));
       umma_commit(&sm.s_full[t]);
     }
     for (int j = 0; j < n_max && ok; ++j) {
@@ -250,7 +285,7 @@ __device__ void mma_role(const Smem& sm, uint32_t tmem, const FwdParams& p) {
           if (!ok) break;
         }
         tc_fence_after();
-        issue_pv<D>(tmem + C::o_col(t), tmem + C::s_col(t), slot_addr(iv), j > 0);
+        pv_product<D, F8>(tmem + C::o_col(t), tmem + C::s_col(t), slot_addr(iv), j > 0);
         if (j + 1 < nt) {
           if (!k_next) {
             ok = wait_kv(ik);
@@ -260,7 +295,7 @@ __device__ void mma_role(const Smem& sm, uint32_t tmem, const FwdParams& p) {
           }
           // issued after P V of the same tile: the tensor pipe runs them in order,
           // so P is read before the new S overwrites those columns
-          issue_qk<D>(tmem + C::s_col(t), t ? qa1 : qa0, slot_addr(ik));
+          qk_product<D, F8>(tmem + C::s_col(t), t ? qa1 : qa0, slot_addr(ik));
           umma_commit(&sm.s_full[t]);
         } else {
           umma_commit(&sm.o_full[t]);
@@ -287,26 +322,26 @@ __device__ __forceinline__ int last_reader(const Item& it, int j) { return (it.n
 //   V_(j-1)  is free when the next S of its last reader is done (the last V of
 //            a tile is released after that tile's final O += P V instead),
 //   Q_t      is free when the item's last S_t is done.
-template <int D>
+template <int D, bool F8>
 __device__ __forceinline__ void release_after_s(const Smem& sm, const Item& it, int t, int j, uint32_t ring_base) {
-  using C = Cfg<D>;
+  using C = Cfg<D, F8>;
   if (last_reader(it, j) == t) mbar_arrive(&sm.kv_empty[(ring_base + 2 * j) % C::kStages]);
   if (j > 0 && last_reader(it, j - 1) == t) mbar_arrive(&sm.kv_empty[(ring_base + 2 * (j - 1) + 1) % C::kStages]);
   if (j == it.n(t) - 1) mbar_arrive(&sm.q_empty[t]);
 }
 
 // ---------------------------------------------------------------- softmax + epilogue (128 threads per tile)
-template <int D>
+template <int D, bool F8>
 __device__ void softmax_role(const Smem& sm, uint32_t tmem, const FwdParams& p, int warp, int lane) {
-  using C = Cfg<D>;
+  using C = Cfg<D, F8>;
   const int t = warp >> 2;
   const int quarter = warp & 3;  // this warp may touch TMEM lanes [32*quarter, 32*quarter+32)
   const int row = quarter * 32 + lane;
   const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
   const uint32_t s_tm = tmem + lane_base + C::s_col(t);
   const uint32_t o_tm = tmem + lane_base + C::o_col(t);
-  const float sl2 = p.scale_log2;
-  const uint64_t sl2x2 = f2_pack(sl2, sl2);
+  float sl2 = p.scale_log2;
+  uint64_t sl2x2 = f2_pack(sl2, sl2);
   uint32_t s_cnt = 0;  // s_full phases consumed
   uint32_t o_cnt = 0;  // o_full phases consumed
   bool ok = true;
@@ -327,8 +362,14 @@ __device__ void softmax_role(const Smem& sm, uint32_t tmem, const FwdParams& p, 
       ++s_cnt;
       ok = __all_sync(kFull, ok);
       if (!ok) break;
-      if (releaser) release_after_s<D>(sm, it, t, j, ring_base);
+      if (releaser) release_after_s<D, F8>(sm, it, t, j, ring_base);
       tc_fence_after();
+      if constexpr (F8) {
+        // block-wise scales of the e4m3 inputs: Q tile and K tile j of this head
+        const size_t sb = static_cast<size_t>(it.bh) * p.tiles;
+        sl2 = p.scale_log2 * __ldg(p.sq + sb + (it.q0 / kBM) + t) * __ldg(p.sk + sb + j);
+        sl2x2 = f2_pack(sl2, sl2);
+      }
 
       // Pass 1: row maximum of the raw scores, 64 columns at a time (scale > 0,
       // so the maximum commutes with the scaling).
@@ -399,15 +440,29 @@ __device__ void softmax_role(const Smem& sm, uint32_t tmem, const FwdParams& p, 
           r[2 * i] = __float_as_uint(ex2_approx(x0));
           r[2 * i + 1] = __float_as_uint(ex2_approx(x1));
         }
-        uint32_t pk[32];
+        if constexpr (F8) {
+          // e4m3 P: four keys per column, keys [64h, 64h + 64) to columns [16h, 16h + 16)
+          uint32_t pk[16];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const float p0 = __uint_as_float(r[2 * i]);
-          const float p1 = __uint_as_float(r[2 * i + 1]);
-          acc[i & 3] = f2_add(acc[i & 3], f2_pack(p0, p1));
-          pk[i] = pack_bf16x2(p0, p1);
+          for (int i = 0; i < 16; ++i) {
+            const float p0 = __uint_as_float(r[4 * i]), p1 = __uint_as_float(r[4 * i + 1]);
+            const float p2 = __uint_as_float(r[4 * i + 2]), p3 = __uint_as_float(r[4 * i + 3]);
+            acc[(2 * i) & 3] = f2_add(acc[(2 * i) & 3], f2_pack(p0, p1));
+            acc[(2 * i + 1) & 3] = f2_add(acc[(2 * i + 1) & 3], f2_pack(p2, p3));
+            pk[i] = pack_e4m3x2(p0, p1) | (pack_e4m3x2(p2, p3) << 16);
+          }
+          tmem_st_x16(s_tm + 16 * h, pk);
+        } else {
+          uint32_t pk[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const float p0 = __uint_as_float(r[2 * i]);
+            const float p1 = __uint_as_float(r[2 * i + 1]);
+            acc[i & 3] = f2_add(acc[i & 3], f2_pack(p0, p1));
+            pk[i] = pack_bf16x2(p0, p1);
+          }
+          tmem_st_x32(s_tm + 32 * h, pk);
         }
-        tmem_st_x32(s_tm + 32 * h, pk);
       }
       float s0, s1, s2, s3;
       f2_unpack(f2_add(acc[0], acc[1]), s0, s1);
@@ -428,7 +483,8 @@ __device__ void softmax_role(const Smem& sm, uint32_t tmem, const FwdParams& p, 
     tc_fence_after();
 
     // Epilogue: O / l to bf16 in registers, release O's TMEM columns, then store.
-    const float inv_l = 1.f / l;
+    // (e4m3 V: O carries V's per-head scale)
+    const float inv_l = (F8 ? __ldg(p.sv + it.bh) : 1.f) / l;
     const uint64_t inv_l2 = f2_pack(inv_l, inv_l);
     uint32_t w[D / 2];
 #pragma unroll
@@ -453,13 +509,13 @@ __device__ void softmax_role(const Smem& sm, uint32_t tmem, const FwdParams& p, 
   }
 }
 
-template <int D>
+template <int D, bool F8>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
-  using C = Cfg<D>;
+  using C = Cfg<D, F8>;
   extern __shared__ uint8_t smem_raw[];
-  const Smem sm = carve<D>(smem_raw);
+  const Smem sm = carve<D, F8>(smem_raw);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
@@ -490,11 +546,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *sm.tmem_slot;
 
   if (warp == kLoadWarp) {
-    if (lane == 0) load_role<D>(&tm_q, &tm_k, &tm_v, sm, p);
+    if (lane == 0) load_role<D, F8>(&tm_q, &tm_k, &tm_v, sm, p);
   } else if (warp == kMmaWarp) {
-    if (lane == 0) mma_role<D>(sm, tmem, p);
+    if (lane == 0) mma_role<D, F8>(sm, tmem, p);
   } else {
-    softmax_role<D>(sm, tmem, p, warp, lane);
+    softmax_role<D, F8>(sm, tmem, p, warp, lane);
   }
 
   tc_fence_before();
@@ -506,34 +562,27 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int D>
-fa_status launch(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int causal,
-                 float scale, cudaStream_t stream, unsigned int* err, int num_sms) {
-  using C = Cfg<D>;
-  CUtensorMap tq, tk, tv;
+template <int D, bool F8>
+fa_status launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, FwdParams prm, int B, int H,
+                 int N, int causal, float scale, cudaStream_t stream, int num_sms) {
+  using C = Cfg<D, F8>;
   const uint64_t bh = static_cast<uint64_t>(B) * H;
-  if (!encode_bf16_map(&tq, q, D, N, bh, kBM) || !encode_bf16_map(&tk, k, D, N, bh, kBN) ||
-      !encode_bf16_map(&tv, v, D, N, bh, kBN))
-    return FA_ERR_CUDA;
   const int num_pairs = (N + 2 * kBM - 1) / (2 * kBM);
   const long long items = static_cast<long long>(bh) * num_pairs;
-  FwdParams prm;
-  prm.o = static_cast<__nv_bfloat16*>(o);
-  prm.lse = lse;
-  prm.err = err;
   prm.N = N;
   prm.BH = static_cast<int>(bh);
   prm.num_pairs = num_pairs;
   prm.num_items = static_cast<int>(items);
   prm.causal = causal ? 1 : 0;
   prm.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
-  cudaError_t e = cudaFuncSetAttribute(fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+  prm.tiles = (N + kBM - 1) / kBM;
+  cudaError_t e = cudaFuncSetAttribute(fwd_kernel<D, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) {
     set_error_text("cudaFuncSetAttribute(fwd_kernel)", e);
     return FA_ERR_CUDA;
   }
   const int grid = static_cast<int>(items < num_sms ? items : num_sms);
-  fwd_kernel<D><<<grid, kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, prm);
+  fwd_kernel<D, F8><<<grid, kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, prm);
   e = cudaGetLastError();
   if (e != cudaSuccess) {
     set_error_text("fwd_kernel launch", e);
@@ -542,13 +591,48 @@ fa_status launch(const void* q, const void* k, const void* v, void* o, float* ls
   return FA_OK;
 }
 
+template <int D>
+fa_status launch_bf16(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
+                      int causal, float scale, cudaStream_t stream, unsigned int* err, int num_sms) {
+  CUtensorMap tq, tk, tv;
+  const uint64_t bh = static_cast<uint64_t>(B) * H;
+  if (!encode_bf16_map(&tq, q, D, N, bh, kBM) || !encode_bf16_map(&tk, k, D, N, bh, kBN) ||
+      !encode_bf16_map(&tv, v, D, N, bh, kBN))
+    return FA_ERR_CUDA;
+  FwdParams prm{};
+  prm.o = static_cast<__nv_bfloat16*>(o);
+  prm.lse = lse;
+  prm.err = err;
+  return launch<D, false>(tq, tk, tv, prm, B, H, N, causal, scale, stream, num_sms);
+}
+
 }  // namespace
 
 fa_status launch_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
                      int causal, float scale, cudaStream_t stream, unsigned int* err, int num_sms) {
-  if (d == 128) return launch<128>(q, k, v, o, lse, B, H, N, causal, scale, stream, err, num_sms);
-  if (d == 64) return launch<64>(q, k, v, o, lse, B, H, N, causal, scale, stream, err, num_sms);
+  if (d == 128) return launch_bf16<128>(q, k, v, o, lse, B, H, N, causal, scale, stream, err, num_sms);
+  if (d == 64) return launch_bf16<64>(q, k, v, o, lse, B, H, N, causal, scale, stream, err, num_sms);
   return FA_ERR_UNSUPPORTED;
+}
+
+fa_status launch_fwd_fp8(const void* q8, const void* k8, const void* vt8, const float* q_scale, const float* k_scale,
+                         const float* v_scale, void* o, float* lse, int B, int H, int N, int d, int causal,
+                         float scale, int v_pitch, cudaStream_t stream, unsigned int* err, int num_sms) {
+  if (d != 128) return FA_ERR_UNSUPPORTED;
+  CUtensorMap tq, tk, tv;
+  const uint64_t bh = static_cast<uint64_t>(B) * H;
+  // Q, K: [BH][N][128] bytes; V^T: [BH][128][v_pitch] bytes, keys inner
+  if (!encode_u8_map(&tq, q8, 128, N, bh, kBM, 128) || !encode_u8_map(&tk, k8, 128, N, bh, kBN, 128) ||
+      !encode_u8_map(&tv, vt8, N, 128, bh, 128, static_cast<uint64_t>(v_pitch)))
+    return FA_ERR_CUDA;
+  FwdParams prm{};
+  prm.o = static_cast<__nv_bfloat16*>(o);
+  prm.lse = lse;
+  prm.err = err;
+  prm.sq = q_scale;
+  prm.sk = k_scale;
+  prm.sv = v_scale;
+  return launch<128, true>(tq, tk, tv, prm, B, H, N, causal, scale, stream, num_sms);
 }
 
 }  // namespace fa

@@ -33,6 +33,16 @@ unsigned int* device_error_word();
 fa_status launch_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
                      int causal, float scale, cudaStream_t stream, unsigned int* err, int num_sms);
 
+// e4m3 block quantization (d = 128); amax_ws: fp32 [B*H][ceil(N/128)] scratch.
+fa_status launch_quantize_fp8(const void* x, const float* signs, void* codes, float* scales, int B, int H, int N,
+                              int per_head, int transpose, int v_pitch, float* amax_ws, cudaStream_t stream);
+
+// The e4m3 forward (d = 128): q8, k8 [B*H][N][128] bytes, vt8 [B*H][128][v_pitch]
+// bytes, scales [B*H][ceil(N/128)] for Q and K and [B*H] for V.
+fa_status launch_fwd_fp8(const void* q8, const void* k8, const void* vt8, const float* q_scale, const float* k_scale,
+                         const float* v_scale, void* o, float* lse, int B, int H, int N, int d, int causal,
+                         float scale, int v_pitch, cudaStream_t stream, unsigned int* err, int num_sms);
+
 fa_status launch_decode(const void* q, const void* k_cache, const void* v_cache, const int32_t* seqlens, void* o,
                         float* lse, int B, int H, int L, int d, int num_splits, float* ws_o, float* ws_lse,
                         cudaStream_t stream);

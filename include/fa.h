@@ -71,6 +71,53 @@ fa_status fa_fwd(const void *q, const void *k, const void *v, void *o, float *ls
                  int causal, float scale, fa_stream_t stream);
 
 /*
+ * FP8 (e4m3) block quantization for fa_fwd_fp8, with incoherent processing.
+ *
+ * Defines: "已有的几种大模型上下文支持情况" (cicada blog) §4.4 (FA-3's FP8
+ *   support): §4.4.1 every tile entering a tensor-core product has its own
+ *   scale factor; §4.4.2 Q and K are multiplied by a random orthogonal matrix
+ *   R (a Hadamard matrix with random signs) so that outlier dimensions are
+ *   spread out, leaving the scores unchanged: (QR)(KR)^T = Q K^T.
+ *
+ *   x       bf16 [B][H][N][d], d = 128 (FA_ERR_UNSUPPORTED otherwise).
+ *   signs   fp32 [d] of +1 / -1, or NULL for no rotation. With signs, row x
+ *           becomes x R with R = diag(signs) H_d / sqrt(d) (H_d Sylvester-
+ *           Hadamard). Use the same signs for Q and K, none for V.
+ *   codes   e4m3 bytes: [B][H][N][d] (transpose = 0) or [B][H][d][v_pitch]
+ *           (transpose = 1, V^T for fa_fwd_fp8; v_pitch >= N, a multiple of 16;
+ *           bytes beyond N in a row are not written).
+ *   scales  fp32: [B][H][ceil(N/128)] (per_head = 0, one per 128-row tile) or
+ *           [B][H] (per_head = 1). scale = max |value| / 448 over the tile
+ *           (1 for an all-zero tile); code = e4m3(value / scale), rounded to
+ *           nearest even, saturating.
+ * Workspace: B*H*ceil(N/128)*4 bytes of stream-ordered device memory.
+ * Errors: as fa_fwd.
+ */
+fa_status fa_quantize_fp8(const void *x, const float *signs, void *codes, float *scales, int B, int H, int N, int d,
+                          int per_head, int transpose, int v_pitch, fa_stream_t stream);
+
+/*
+ * FP8 prefill forward (FA-3 style, "已有的几种大模型上下文支持情况" §4.4).
+ *
+ *   q8, k8   e4m3 [B][H][N][128] (rotated by the same R), tile scales
+ *            q_scale, k_scale fp32 [B][H][ceil(N/128)] (fa_quantize_fp8,
+ *            per_head = 0).
+ *   vt8      e4m3 V^T [B][H][128][v_pitch], v_scale fp32 [B][H]
+ *            (fa_quantize_fp8, per_head = 1, transpose = 1).
+ *   o, lse, B, H, N, causal, scale: as fa_fwd; d must be 128.
+ * Computes softmax(scale * Q^ K^T [+ causal mask]) V^ over the dequantized
+ * inputs, with both products on e4m3 tensor cores: S tiles carry the product
+ * of their Q and K tile scales, P is rounded to e4m3 for the P V product (the
+ * normaliser l sums the fp32 values), O carries V's scale. An approximation of
+ * fa_fwd: the e4m3 rounding of P is its only error beyond the inputs'.
+ * Errors: as fa_fwd; FA_ERR_INVALID_ARG also for v_pitch < N or not a
+ * multiple of 16.
+ */
+fa_status fa_fwd_fp8(const void *q8, const void *k8, const void *vt8, const float *q_scale, const float *k_scale,
+                     const float *v_scale, void *o, float *lse, int B, int H, int N, int d, int causal, float scale,
+                     int v_pitch, fa_stream_t stream);
+
+/*
  * Backward pass (gradients of fa_fwd) with recomputation.
  *
  * Defines: CMU 15-779 Lecture 5 notes §7.1-7.4 and "FlashAttention 完全拆解

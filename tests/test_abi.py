@@ -194,3 +194,26 @@ def test_decode_gqa_rejects_bad_arguments(lib):
     assert dec(q=None) == fa.FA_ERR_INVALID_ARG
     assert dec(L=0) == fa.FA_ERR_INVALID_ARG
     assert dec(d=96) == fa.FA_ERR_UNSUPPORTED
+
+
+def test_fp8_calls_reject_bad_arguments(lib):
+    import exact_attention_29_gb300 as fa
+
+    def quant(d=128, N=300, per_head=0, transpose=0, pitch=0, x=16):
+        return lib.fa_quantize_fp8(x, None, 16, 16, 1, 1, N, d, per_head, transpose, pitch, None)
+
+    assert quant(x=None) == fa.FA_ERR_INVALID_ARG
+    assert quant(N=0) == fa.FA_ERR_INVALID_ARG
+    assert quant(per_head=2) == fa.FA_ERR_INVALID_ARG
+    assert quant(transpose=1, pitch=296) == fa.FA_ERR_INVALID_ARG  # below N
+    assert quant(transpose=1, pitch=308) == fa.FA_ERR_INVALID_ARG  # not a multiple of 16
+    assert quant(d=64) == fa.FA_ERR_UNSUPPORTED
+
+    def fwd(d=128, N=300, pitch=304, scale=0.1, causal=0):
+        return lib.fa_fwd_fp8(16, 16, 16, 16, 16, 16, 16, 16, 1, 1, N, d, causal, scale, pitch, None)
+
+    assert fwd(pitch=296) == fa.FA_ERR_INVALID_ARG
+    assert fwd(pitch=300) == fa.FA_ERR_INVALID_ARG
+    assert fwd(scale=0.0) == fa.FA_ERR_INVALID_ARG
+    assert fwd(causal=5) == fa.FA_ERR_INVALID_ARG
+    assert fwd(d=64) == fa.FA_ERR_UNSUPPORTED
