@@ -33,6 +33,7 @@ def main():
     ap.add_argument("--batch", type=int, default=0)
     ap.add_argument("--splits", type=int, default=16)
     ap.add_argument("--bwd", action="store_true", help="time fa_bwd (after one fa_fwd) on a prefill workload")
+    ap.add_argument("--fp8", action="store_true", help="time fa_fwd_fp8 on e4m3 inputs of a prefill workload")
     args = ap.parse_args()
     build.build()
     dev = torch.device("cuda:0")
@@ -46,6 +47,16 @@ def main():
 
         def run():
             fa.fa_fwd(q, k, v, causal=c.causal, o=o, lse=lse, stream=stream)
+
+        if args.fp8:
+            g = torch.Generator().manual_seed(1)
+            signs = (torch.randint(0, 2, (c.d,), generator=g) * 2 - 1).float().to(dev)
+            q8, qs = fa.fa_quantize_fp8(q, signs)
+            k8, ks = fa.fa_quantize_fp8(k, signs)
+            vt8, vs = fa.fa_quantize_fp8(v, None, per_head=True, transpose=True)
+
+            def run():
+                fa.fa_fwd_fp8(q8, k8, vt8, qs, ks, vs, causal=c.causal, o=o, lse=lse, stream=stream)
 
         if args.bwd:
             run()
@@ -95,7 +106,7 @@ def main():
 
         kv = perfmodel.decode_kv_bytes(c.Hkv if hasattr(c, "Hkv") else c.H, c.d, sl.tolist())
         extra = f" best {kv / min(times) / 1e6:.0f} GB/s of K/V"
-    what = "bwd" if args.bwd else "fwd"
+    what = "bwd" if args.bwd else ("fwd_fp8" if args.fp8 else "fwd")
     print(f"{args.workload} {what if args.workload in wl.PREFILL else ''} B={B}: "
           + " ".join(f"{t:.3f}ms" for t in times) + extra)
 
