@@ -68,6 +68,9 @@ def _load():
             lib.oracle_attention.restype = ctypes.c_int
             lib.oracle_decode.argtypes = [dp, dp, dp, ip, dp, dp] + [ctypes.c_int] * 4
             lib.oracle_decode.restype = ctypes.c_int
+            lib.oracle_attention_block_mask.argtypes = [dp, dp, dp, ctypes.POINTER(ctypes.c_ubyte), ctypes.c_int,
+                                                         ctypes.c_int, dp, dp] + [ctypes.c_int] * 5 + [ctypes.c_double]
+            lib.oracle_attention_block_mask.restype = ctypes.c_int
             lib.oracle_decode_gqa.argtypes = [dp, dp, dp, ip, dp, dp] + [ctypes.c_int] * 5
             lib.oracle_decode_gqa.restype = ctypes.c_int
             lib.oracle_attention_bwd.argtypes = [dp] * 7 + [ctypes.c_int] * 5 + [ctypes.c_double]
@@ -163,6 +166,29 @@ def decode(q, k_cache, v_cache, seqlens):
     rc = lib.oracle_decode(_ptr(qq), _ptr(kk), _ptr(vv), _ptr(sl, ctypes.c_int), _ptr(o), _ptr(lse),
                            B, H, L, d)
     _check(rc, "decode")
+    return o, lse
+
+
+def attention_block_mask(q, k, v, mask, causal: bool, scale: float, block: int = 128):
+    """Attention of [B, H, N, d] tensors under a block mask [T, T] or
+    [H, T, T] (T = ceil(N / block)); returns (o, lse) as fp64 arrays."""
+    lib = _load()
+    qq, kk, vv = _f64(q), _f64(k), _f64(v)
+    B, H, N, d = qq.shape
+    if hasattr(mask, "detach"):
+        mask = mask.detach().cpu().numpy()
+    mk = np.ascontiguousarray(np.asarray(mask) != 0, dtype=np.uint8)
+    T = (N + block - 1) // block
+    if mk.ndim == 2:
+        mk = mk[None]
+    if mk.shape[1:] != (T, T) or mk.shape[0] not in (1, H):
+        raise ValueError("mask must be [T, T] or [H, T, T]")
+    o = np.empty((B, H, N, d), dtype=np.float64)
+    lse = np.empty((B, H, N), dtype=np.float64)
+    rc = lib.oracle_attention_block_mask(_ptr(qq), _ptr(kk), _ptr(vv), mk.ctypes.data_as(ctypes.POINTER(ctypes.c_ubyte)),
+                                         mk.shape[0], block, _ptr(o), _ptr(lse), B, H, N, d, int(bool(causal)),
+                                         float(scale))
+    _check(rc, "attention_block_mask")
     return o, lse
 
 

@@ -195,6 +195,70 @@ int oracle_decode(const double *q, const double *k_cache, const double *v_cache,
 }
 
 /*
+ * Standard attention under a block mask (block-sparse attention).
+ *
+ *   q, k, v [B][H][N][d]; o [B][H][N][d]; lse [B][H][N];
+ *   mask [mask_heads][T][T] bytes, T = ceil(N / block), mask_heads 1 (one
+ *   mask for every head) or H (head h uses mask h).
+ *
+ * "FlashAttention 完全拆解（一）", block-sparse extension: a block-level mask
+ * over the N x N score matrix; the scores of masked-out blocks take no part.
+ * Key j is visible to query i when mask[i / block][j / block] != 0 and, if
+ * causal, j <= i. Each row is the standard softmax over its visible keys
+ * (max subtracted, exp, sum, divide, O = P V, LSE = m + ln l). A row with no
+ * visible key has o = 0 and lse = -inf (the empty sum; the identity of the
+ * combine operator).
+ */
+int oracle_attention_block_mask(const double *q, const double *k, const double *v,
+                                const unsigned char *mask, int mask_heads, int block,
+                                double *o, double *lse, int B, int H, int N, int d,
+                                int causal, double scale) {
+  if (B < 1 || H < 1 || N < 1 || d < 1 || block < 1) return ORACLE_ERR_ARG;
+  if (mask_heads != 1 && mask_heads != H) return ORACLE_ERR_ARG;
+  int T = (N + block - 1) / block;
+  double *s = (double *)malloc((size_t)N * sizeof(double));
+  if (!s) return ORACLE_ERR_NOMEM;
+  for (int b = 0; b < B; ++b) {
+    for (int h = 0; h < H; ++h) {
+      size_t bh = (size_t)b * H + h;
+      const unsigned char *mk = mask + (size_t)(mask_heads == 1 ? 0 : h) * T * T;
+      const double *qh = q + bh * (size_t)N * d, *kh = k + bh * (size_t)N * d, *vh = v + bh * (size_t)N * d;
+      for (int i = 0; i < N; ++i) {
+        double m = -INFINITY;
+        for (int j = 0; j < N; ++j) {
+          int vis = mk[(size_t)(i / block) * T + (j / block)] != 0 && (!causal || j <= i);
+          if (!vis) {
+            s[j] = -INFINITY;
+            continue;
+          }
+          double acc = 0.0;
+          for (int t = 0; t < d; ++t) acc += qh[(size_t)i * d + t] * kh[(size_t)j * d + t];
+          s[j] = acc * scale;
+          if (s[j] > m) m = s[j];
+        }
+        double *orow = o + (bh * N + i) * (size_t)d;
+        for (int t = 0; t < d; ++t) orow[t] = 0.0;
+        if (m == -INFINITY) {
+          lse[bh * N + i] = -INFINITY;
+          continue;
+        }
+        double l = 0.0;
+        for (int j = 0; j < N; ++j) {
+          if (s[j] == -INFINITY) continue;
+          double e = exp(s[j] - m);
+          l += e;
+          for (int t = 0; t < d; ++t) orow[t] += e * vh[(size_t)j * d + t];
+        }
+        for (int t = 0; t < d; ++t) orow[t] /= l;
+        lse[bh * N + i] = m + log(l);
+      }
+    }
+  }
+  free(s);
+  return ORACLE_OK;
+}
+
+/*
  * Decode with grouped K/V heads (GQA; MQA when H_kv = 1).
  *
  *   q [B][H_q][d]; k_cache, v_cache [B][H_kv][L][d]; seqlens [B];
