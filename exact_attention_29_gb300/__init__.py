@@ -21,6 +21,8 @@ from ._lib import (  # noqa: F401
     fa_decode_noalloc,
     fa_fwd,
     fa_fwd_fp8,
+    fa_fwd_sparse,
+    fa_fwd_sparse_plan,
     fa_quantize_fp8,
     fa_fwd_plan,
     fa_selftest_mma,

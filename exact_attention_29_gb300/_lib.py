@@ -33,6 +33,8 @@ _SIGNATURES = {
     "fa_decode": ([_VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _VP], _I),
     "fa_bwd": ([_VP] * 9 + [_I] * 5 + [ctypes.c_float, _VP], _I),
     "fa_decode_gqa": ([_VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _I, _VP], _I),
+    "fa_fwd_sparse": ([_VP, _VP, _VP, _VP, _I, _VP, _VP] + [_I] * 5 + [ctypes.c_float, _VP], _I),
+    "fa_fwd_sparse_plan": ([_VP] + [_I] * 5 + [ctypes.POINTER(ctypes.c_longlong)] * 2, _I),
     "fa_quantize_fp8": ([_VP, _VP, _VP, _VP] + [_I] * 7 + [_VP], _I),
     "fa_fwd_fp8": ([_VP] * 8 + [_I] * 5 + [ctypes.c_float, _I, _VP], _I),
     "fa_bwd_plan": ([_I, _I, _I, _I, ctypes.POINTER(ctypes.c_longlong)], _I),
@@ -123,6 +125,49 @@ def fa_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = Fal
                     1 if causal else 0, float(scale), _stream_handle(stream))
     _check(st, "fa_fwd")
     return o, lse
+
+
+def fa_fwd_sparse(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, mask: torch.Tensor, causal: bool = False,
+                  scale: float | None = None, o=None, lse=None, stream=None):
+    """Block-sparse forward. q, k, v bf16 [B, H, N, d]; mask uint8 (or bool) on
+    the GPU, [T, T] or [H, T, T] with T = ceil(N / 128).
+
+    Returns (o bf16 [B, H, N, d], lse fp32 [B, H, N]).
+    """
+    lib = load_library()
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _require(t, n, torch.bfloat16, 4)
+    B, H, N, d = q.shape
+    T = (N + 127) // 128
+    mask = mask.to(torch.uint8).contiguous()
+    if mask.dim() == 2:
+        mask = mask.unsqueeze(0)
+    if mask.shape[1:] != (T, T) or mask.shape[0] not in (1, H) or mask.device != q.device:
+        raise ValueError("mask must be [T, T] or [H, T, T] on the device of q, T = ceil(N/128)")
+    if scale is None:
+        scale = d ** -0.5
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    st = lib.fa_fwd_sparse(q.data_ptr(), k.data_ptr(), v.data_ptr(), mask.data_ptr(), mask.shape[0], o.data_ptr(),
+                           lse.data_ptr(), B, H, N, d, 1 if causal else 0, float(scale), _stream_handle(stream))
+    _check(st, "fa_fwd_sparse")
+    return o, lse
+
+
+def fa_fwd_sparse_plan(mask, B: int, H: int, N: int, causal: bool = False):
+    """(pairs_allowed, pairs_computed) of fa_fwd_sparse for a host mask [T, T] or [H, T, T]."""
+    import numpy as np
+
+    lib = load_library()
+    m = np.ascontiguousarray(np.asarray(mask.cpu() if hasattr(mask, "cpu") else mask) != 0, dtype=np.uint8)
+    if m.ndim == 2:
+        m = m[None]
+    a, c = ctypes.c_longlong(0), ctypes.c_longlong(0)
+    _check(lib.fa_fwd_sparse_plan(m.ctypes.data, m.shape[0], B, H, N, 1 if causal else 0, ctypes.byref(a),
+                                  ctypes.byref(c)), "fa_fwd_sparse_plan")
+    return a.value, c.value
 
 
 def _pitch16(n: int) -> int:

@@ -194,6 +194,52 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
                     g_num_sms[dev]);
 }
 
+fa_status fa_fwd_sparse(const void* q, const void* k, const void* v, const uint8_t* mask, int mask_heads, void* o,
+                        float* lse, int B, int H, int N, int d, int causal, float scale, fa_stream_t stream) {
+  if (!q || !k || !v || !mask || !o || !lse) return FA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned4(lse)) return FA_ERR_INVALID_ARG;
+  if (B < 1 || H < 1 || N < 1 || d < 1) return FA_ERR_INVALID_ARG;
+  if (mask_heads != 1 && mask_heads != H) return FA_ERR_INVALID_ARG;
+  if (!(scale > 0.f) || !std::isfinite(scale)) return FA_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  const long long bh = static_cast<long long>(B) * H;
+  const long long pairs = (static_cast<long long>(N) + 255) / 256;
+  if (bh > 0x7fffffffLL || pairs > 65535) return FA_ERR_INVALID_ARG;
+  int dev = -1;
+  fa_status st = current_device(&dev);
+  if (st != FA_OK) return st;
+  unsigned int* err = device_error_word();
+  if (!err) return FA_ERR_CUDA;
+  return launch_fwd_sparse(q, k, v, mask, mask_heads, o, lse, B, H, N, d, causal, scale,
+                           reinterpret_cast<cudaStream_t>(stream), err, g_num_sms[dev]);
+}
+
+fa_status fa_fwd_sparse_plan(const uint8_t* mask, int mask_heads, int B, int H, int N, int causal,
+                             long long* pairs_allowed, long long* pairs_computed) {
+  if (!mask || !pairs_allowed || !pairs_computed || B < 1 || H < 1 || N < 1) return FA_ERR_INVALID_ARG;
+  if (mask_heads != 1 && mask_heads != H) return FA_ERR_INVALID_ARG;
+  const int T = (N + 127) / 128;
+  long long allowed = 0, computed = 0;
+  for (int h = 0; h < H; ++h) {
+    const uint8_t* mk = mask + static_cast<size_t>(mask_heads == 1 ? 0 : h) * T * T;
+    auto ok = [&](int i, int j) { return (!causal || j <= i) && mk[static_cast<size_t>(i) * T + j] != 0; };
+    for (int i = 0; i < T; ++i)
+      for (int j = 0; j < T; ++j) allowed += ok(i, j) ? 1 : 0;
+    // the kernel walks, for each pair of Q tiles, the union of their K/V tiles
+    // (at least one step, fully masked when the union is empty)
+    for (int i0 = 0; i0 < T; i0 += 2) {
+      const bool has1 = i0 + 1 < T;
+      long long nu = 0;
+      for (int j = 0; j < T; ++j) nu += (ok(i0, j) || (has1 && ok(i0 + 1, j))) ? 1 : 0;
+      computed += (nu > 0 ? nu : 1) * (has1 ? 2 : 1);
+    }
+  }
+  *pairs_allowed = allowed * B;
+  *pairs_computed = computed * B;
+  return FA_OK;
+}
+
 fa_status fa_quantize_fp8(const void* x, const float* signs, void* codes, float* scales, int B, int H, int N, int d,
                           int per_head, int transpose, int v_pitch, fa_stream_t stream) {
   if (!x || !codes || !scales) return FA_ERR_INVALID_ARG;

@@ -30,6 +30,11 @@
 //   TMEM A operand of O += P V. While warpgroup 0 runs the softmax of S0 the
 //   tensor core works on tile 1's products, and the other way round.
 //
+// With a block mask (block-sparse FlashAttention, "FlashAttention 完全拆解
+// （一）", block-sparse extension) an item's two Q tiles walk the union of
+// the K/V tiles their masks keep; tiles outside the union are never loaded or
+// multiplied.
+//
 // The same kernel runs the FP8 path ("已有的几种大模型上下文支持情况" §4.4,
 // FA-3): e4m3 Q and K with one scale per 128-row tile (the product of the two
 // tile scales joins the softmax scale of each S tile), V given transposed as
@@ -87,6 +92,10 @@ struct FwdParams {
   const float* sk;
   const float* sv;
   int tiles;
+  // block-sparse mode only: mask [mask_heads][tiles][tiles] bytes (nullptr: dense)
+  const uint8_t* mask;
+  int mask_heads;
+  int H;
   int N;
   int BH;          // batch * heads
   int num_pairs;   // Q-tile pairs per head
@@ -135,7 +144,20 @@ __device__ __forceinline__ Smem carve(uint8_t* raw) {
   return s;
 }
 
+// Block-sparse mode ("FlashAttention 完全拆解（一）", block-sparse extension):
+// K/V tile j takes part for Q tile qi when the block mask allows it and, under
+// the causal mask, j <= qi (square tiles).
+__device__ __forceinline__ bool tile_allowed(const FwdParams& p, int bh, int qi, int j) {
+  if (p.causal && j > qi) return false;
+  const int mh = (p.mask_heads == 1) ? 0 : (bh % p.H);
+  return p.mask[(static_cast<size_t>(mh) * p.tiles + qi) * p.tiles + j] != 0;
+}
+
 // One work item: Q rows [q0, q0 + 256) of head bh; tile t visits n(t) K/V tiles.
+// Dense: tile t visits K/V tiles 0 .. n(t)-1. Block-sparse: both tiles walk the
+// union of their allowed K/V tiles in increasing order (a step that one tile's
+// mask removes is fully masked for that tile); an item whose union is empty
+// walks tile 0 fully masked, so its rows still get o = 0, lse = -inf.
 struct Item {
   int bh;
   int q0;
@@ -145,7 +167,32 @@ struct Item {
   __device__ __forceinline__ int n_max() const { return n0 > n1 ? n0 : n1; }
 };
 
+// Next K/V tile >= j in the item's union (p.tiles if none).
+__device__ __forceinline__ int union_next(const FwdParams& p, const Item& it, int j) {
+  const int qi0 = it.q0 / kBM;
+  const bool has1 = it.q0 + kBM < p.N;
+  for (; j < p.tiles; ++j)
+    if (tile_allowed(p, it.bh, qi0, j) || (has1 && tile_allowed(p, it.bh, qi0 + 1, j))) return j;
+  return p.tiles;
+}
+
+// K/V tile of the first step of an item.
+template <bool SP>
+__device__ __forceinline__ int first_kv(const FwdParams& p, const Item& it) {
+  if constexpr (!SP) return 0;
+  const int j = union_next(p, it, 0);
+  return j < p.tiles ? j : 0;
+}
+
+// K/V tile of the step after the one on tile j.
+template <bool SP>
+__device__ __forceinline__ int next_kv(const FwdParams& p, const Item& it, int j) {
+  if constexpr (!SP) return j + 1;
+  return union_next(p, it, j + 1);
+}
+
 // k-th item of this CTA (snake order over the heavy-first item list), or false.
+template <bool SP>
 __device__ __forceinline__ bool item_at(const FwdParams& p, int k, Item& it) {
   const int G = static_cast<int>(gridDim.x);
   const int c = static_cast<int>(blockIdx.x);
@@ -155,13 +202,21 @@ __device__ __forceinline__ bool item_at(const FwdParams& p, int k, Item& it) {
   it.bh = static_cast<int>(w - static_cast<long long>(rank) * p.BH);
   const int pair = p.causal ? (p.num_pairs - 1 - rank) : rank;
   it.q0 = pair * 2 * kBM;
-  it.n0 = fwd_kv_tiles(it.q0, p.N, kBN, p.causal);
-  it.n1 = fwd_kv_tiles(it.q0 + kBM, p.N, kBN, p.causal);
+  if constexpr (!SP) {
+    it.n0 = fwd_kv_tiles(it.q0, p.N, kBN, p.causal);
+    it.n1 = fwd_kv_tiles(it.q0 + kBM, p.N, kBN, p.causal);
+  } else {
+    int nu = 0;
+    for (int j = union_next(p, it, 0); j < p.tiles; j = union_next(p, it, j + 1)) ++nu;
+    if (nu == 0) nu = 1;
+    it.n0 = nu;
+    it.n1 = (it.q0 + kBM < p.N) ? nu : 0;
+  }
   return true;
 }
 
 // ---------------------------------------------------------------- TMA producer (one thread)
-template <int D, bool F8>
+template <int D, bool F8, bool SP>
 __device__ void load_role(const CUtensorMap* tm_q, const CUtensorMap* tm_k, const CUtensorMap* tm_v, const Smem& sm,
                           const FwdParams& p) {
   using C = Cfg<D, F8>;
@@ -172,7 +227,7 @@ __device__ void load_role(const CUtensorMap* tm_q, const CUtensorMap* tm_k, cons
   uint32_t q_cnt[2] = {0, 0};   // Q tiles issued per buffer
   bool ok = true;
   Item it;
-  for (int k = 0; ok && item_at(p, k, it); ++k) {
+  for (int k = 0; ok && item_at<SP>(p, k, it); ++k) {
     for (int t = 0; t < 2 && ok; ++t) {
       if (it.n(t) == 0) continue;
       if (q_cnt[t] > 0) {
@@ -186,7 +241,8 @@ __device__ void load_role(const CUtensorMap* tm_q, const CUtensorMap* tm_k, cons
       ++q_cnt[t];
     }
     const int n_max = it.n_max();
-    for (int j = 0; j < n_max && ok; ++j) {
+    int jt = first_kv<SP>(p, it);  // K/V tile of step j
+    for (int j = 0; j < n_max && ok; ++j, jt = next_kv<SP>(p, it, jt)) {
       for (int kind = 0; kind < 2; ++kind) {
         const uint32_t slot = ring % C::kStages;
         const uint32_t use = ring / C::kStages;
@@ -198,12 +254,12 @@ __device__ void load_role(const CUtensorMap* tm_q, const CUtensorMap* tm_k, cons
         mbar_arrive_expect_tx(&sm.kv_full[slot], C::kTileBytes);
         const CUtensorMap* map = kind ? tm_v : tm_k;
         if (F8 && kind) {
-          // V^T: rows are d, the 128 keys of tile j are the inner coordinate
-          tma_load_3d(dst, map, &sm.kv_full[slot], j * kBN, 0, it.bh);
+          // V^T: rows are d, the 128 keys of tile jt are the inner coordinate
+          tma_load_3d(dst, map, &sm.kv_full[slot], jt * kBN, 0, it.bh);
         } else {
 #pragma unroll
           for (int c = 0; c < C::kChunks; ++c)
-            tma_load_3d(dst + c * kChunkBytes, map, &sm.kv_full[slot], c * 64, j * kBN, it.bh);
+            tma_load_3d(dst + c * kChunkBytes, map, &sm.kv_full[slot], c * 64, jt * kBN, it.bh);
         }
         ++ring;
       }
@@ -233,7 +289,7 @@ __device__ __forceinline__ void pv_product(uint32_t o_tmem, uint32_t p_tmem, uin
     issue_pv<D>(o_tmem, p_tmem, v_smem, accumulate);
 }
 
-template <int D, bool F8>
+template <int D, bool F8, bool SP>
 __device__ void mma_role(const Smem& sm, uint32_t tmem, const FwdParams& p) {
   using C = Cfg<D, F8>;
   const uint32_t ring_base = smem_u32(sm.ring);
@@ -249,7 +305,7 @@ __device__ void mma_role(const Smem& sm, uint32_t tmem, const FwdParams& p) {
   uint32_t o_cnt[2] = {0, 0};        // items whose O_t was produced
   bool ok = true;
   Item it;
-  for (int k = 0; ok && item_at(p, k, it); ++k) {
+  for (int k = 0; ok && item_at<SP>(p, k, it); ++k) {
     for (int t = 0; t < 2 && ok; ++t) {
       if (it.n(t) == 0) continue;
       ok = bounded_wait(&sm.q_full[t], q_cnt[t] & 1, sm.abort_flag, p.err, kSiteQFull);
@@ -331,7 +387,7 @@ __device__ __forceinline__ void release_after_s(const Smem& sm, const Item& it, 
 }
 
 // ---------------------------------------------------------------- softmax + epilogue (128 threads per tile)
-template <int D, bool F8>
+template <int D, bool F8, bool SP>
 __device__ void softmax_role(const Smem& sm, uint32_t tmem, const FwdParams& p, int warp, int lane) {
   using C = Cfg<D, F8>;
   const int t = warp >> 2;
@@ -348,7 +404,7 @@ __device__ void softmax_role(const Smem& sm, uint32_t tmem, const FwdParams& p, 
   Item it;
   const bool releaser = (quarter == 0 && lane == 0);  // one thread per tile releases buffers
   uint32_t ring_next = 0;                             // K/V ring position of the next item
-  for (int k = 0; ok && item_at(p, k, it); ++k) {
+  for (int k = 0; ok && item_at<SP>(p, k, it); ++k) {
     const uint32_t ring_base = ring_next;  // K_j is ring_base + 2j, V_j is ring_base + 2j + 1
     ring_next += 2 * it.n_max();
     const int nkv = it.n(t);
@@ -357,7 +413,8 @@ __device__ void softmax_role(const Smem& sm, uint32_t tmem, const FwdParams& p, 
     const int vis_end = p.causal ? min(q_row + 1, p.N) : p.N;  // keys [0, vis_end) are visible to this row
     float m_used = -INFINITY;  // base of every exponent so far (log2 domain, scaled)
     float l = 0.f;
-    for (int j = 0; j < nkv; ++j) {
+    int jt = first_kv<SP>(p, it);  // K/V tile of step j
+    for (int j = 0; j < nkv; ++j, jt = next_kv<SP>(p, it, jt)) {
       ok = bounded_wait(&sm.s_full[t], s_cnt & 1, sm.abort_flag, p.err, kSiteSFull);
       ++s_cnt;
       ok = __all_sync(kFull, ok);
@@ -367,13 +424,14 @@ __device__ void softmax_role(const Smem& sm, uint32_t tmem, const FwdParams& p, 
       if constexpr (F8) {
         // block-wise scales of the e4m3 inputs: Q tile and K tile j of this head
         const size_t sb = static_cast<size_t>(it.bh) * p.tiles;
-        sl2 = p.scale_log2 * __ldg(p.sq + sb + (it.q0 / kBM) + t) * __ldg(p.sk + sb + j);
+        sl2 = p.scale_log2 * __ldg(p.sq + sb + (it.q0 / kBM) + t) * __ldg(p.sk + sb + jt);
         sl2x2 = f2_pack(sl2, sl2);
       }
 
       // Pass 1: row maximum of the raw scores, 64 columns at a time (scale > 0,
       // so the maximum commutes with the scaling).
-      const int lim = vis_end - j * kBN;  // visible keys of this tile for this row
+      // visible keys of this tile for this row (none when the block mask removes it)
+      const int lim = (SP && !tile_allowed(p, it.bh, it.q0 / kBM + t, jt)) ? 0 : vis_end - jt * kBN;
       float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
@@ -484,7 +542,8 @@ __device__ void softmax_role(const Smem& sm, uint32_t tmem, const FwdParams& p, 
 
     // Epilogue: O / l to bf16 in registers, release O's TMEM columns, then store.
     // (e4m3 V: O carries V's per-head scale)
-    const float inv_l = (F8 ? __ldg(p.sv + it.bh) : 1.f) / l;
+    // (a row that saw no key, possible under a block mask: o = 0, lse = -inf)
+    const float inv_l = (l > 0.f) ? (F8 ? __ldg(p.sv + it.bh) : 1.f) / l : 0.f;
     const uint64_t inv_l2 = f2_pack(inv_l, inv_l);
     uint32_t w[D / 2];
 #pragma unroll
@@ -504,12 +563,12 @@ __device__ void softmax_role(const Smem& sm, uint32_t tmem, const FwdParams& p, 
       uint4* dst = reinterpret_cast<uint4*>(p.o + (static_cast<size_t>(it.bh) * p.N + q_row) * D);
 #pragma unroll
       for (int i = 0; i < D / 8; ++i) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
-      p.lse[static_cast<size_t>(it.bh) * p.N + q_row] = (m_used + log2f(l)) * kLn2;
+      p.lse[static_cast<size_t>(it.bh) * p.N + q_row] = (l > 0.f) ? (m_used + log2f(l)) * kLn2 : -INFINITY;
     }
   }
 }
 
-template <int D, bool F8>
+template <int D, bool F8, bool SP>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
@@ -546,11 +605,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *sm.tmem_slot;
 
   if (warp == kLoadWarp) {
-    if (lane == 0) load_role<D, F8>(&tm_q, &tm_k, &tm_v, sm, p);
+    if (lane == 0) load_role<D, F8, SP>(&tm_q, &tm_k, &tm_v, sm, p);
   } else if (warp == kMmaWarp) {
-    if (lane == 0) mma_role<D, F8>(sm, tmem, p);
+    if (lane == 0) mma_role<D, F8, SP>(sm, tmem, p);
   } else {
-    softmax_role<D, F8>(sm, tmem, p, warp, lane);
+    softmax_role<D, F8, SP>(sm, tmem, p, warp, lane);
   }
 
   tc_fence_before();
@@ -562,7 +621,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int D, bool F8>
+template <int D, bool F8, bool SP>
 fa_status launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, FwdParams prm, int B, int H,
                  int N, int causal, float scale, cudaStream_t stream, int num_sms) {
   using C = Cfg<D, F8>;
@@ -576,13 +635,15 @@ fa_status launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap
   prm.causal = causal ? 1 : 0;
   prm.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   prm.tiles = (N + kBM - 1) / kBM;
-  cudaError_t e = cudaFuncSetAttribute(fwd_kernel<D, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+  prm.H = H;
+  cudaError_t e = cudaFuncSetAttribute(fwd_kernel<D, F8, SP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       C::kSmemBytes);
   if (e != cudaSuccess) {
     set_error_text("cudaFuncSetAttribute(fwd_kernel)", e);
     return FA_ERR_CUDA;
   }
   const int grid = static_cast<int>(items < num_sms ? items : num_sms);
-  fwd_kernel<D, F8><<<grid, kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, prm);
+  fwd_kernel<D, F8, SP><<<grid, kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, prm);
   e = cudaGetLastError();
   if (e != cudaSuccess) {
     set_error_text("fwd_kernel launch", e);
@@ -593,7 +654,8 @@ fa_status launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap
 
 template <int D>
 fa_status launch_bf16(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
-                      int causal, float scale, cudaStream_t stream, unsigned int* err, int num_sms) {
+                      int causal, float scale, cudaStream_t stream, unsigned int* err, int num_sms,
+                      const uint8_t* mask = nullptr, int mask_heads = 0) {
   CUtensorMap tq, tk, tv;
   const uint64_t bh = static_cast<uint64_t>(B) * H;
   if (!encode_bf16_map(&tq, q, D, N, bh, kBM) || !encode_bf16_map(&tk, k, D, N, bh, kBN) ||
@@ -603,7 +665,10 @@ fa_status launch_bf16(const void* q, const void* k, const void* v, void* o, floa
   prm.o = static_cast<__nv_bfloat16*>(o);
   prm.lse = lse;
   prm.err = err;
-  return launch<D, false>(tq, tk, tv, prm, B, H, N, causal, scale, stream, num_sms);
+  prm.mask = mask;
+  prm.mask_heads = mask_heads;
+  if (mask != nullptr) return launch<D, false, true>(tq, tk, tv, prm, B, H, N, causal, scale, stream, num_sms);
+  return launch<D, false, false>(tq, tk, tv, prm, B, H, N, causal, scale, stream, num_sms);
 }
 
 }  // namespace
@@ -612,6 +677,16 @@ fa_status launch_fwd(const void* q, const void* k, const void* v, void* o, float
                      int causal, float scale, cudaStream_t stream, unsigned int* err, int num_sms) {
   if (d == 128) return launch_bf16<128>(q, k, v, o, lse, B, H, N, causal, scale, stream, err, num_sms);
   if (d == 64) return launch_bf16<64>(q, k, v, o, lse, B, H, N, causal, scale, stream, err, num_sms);
+  return FA_ERR_UNSUPPORTED;
+}
+
+fa_status launch_fwd_sparse(const void* q, const void* k, const void* v, const uint8_t* mask, int mask_heads, void* o,
+                            float* lse, int B, int H, int N, int d, int causal, float scale, cudaStream_t stream,
+                            unsigned int* err, int num_sms) {
+  if (d == 128)
+    return launch_bf16<128>(q, k, v, o, lse, B, H, N, causal, scale, stream, err, num_sms, mask, mask_heads);
+  if (d == 64)
+    return launch_bf16<64>(q, k, v, o, lse, B, H, N, causal, scale, stream, err, num_sms, mask, mask_heads);
   return FA_ERR_UNSUPPORTED;
 }
 
@@ -632,7 +707,7 @@ fa_status launch_fwd_fp8(const void* q8, const void* k8, const void* vt8, const 
   prm.sq = q_scale;
   prm.sk = k_scale;
   prm.sv = v_scale;
-  return launch<128, true>(tq, tk, tv, prm, B, H, N, causal, scale, stream, num_sms);
+  return launch<128, true, false>(tq, tk, tv, prm, B, H, N, causal, scale, stream, num_sms);
 }
 
 }  // namespace fa

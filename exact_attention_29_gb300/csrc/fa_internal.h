@@ -37,6 +37,11 @@ fa_status launch_fwd(const void* q, const void* k, const void* v, void* o, float
 fa_status launch_quantize_fp8(const void* x, const float* signs, void* codes, float* scales, int B, int H, int N,
                               int per_head, int transpose, int v_pitch, float* amax_ws, cudaStream_t stream);
 
+// Block-sparse forward: mask [mask_heads][T][T] bytes on the device, T = ceil(N / 128).
+fa_status launch_fwd_sparse(const void* q, const void* k, const void* v, const uint8_t* mask, int mask_heads, void* o,
+                            float* lse, int B, int H, int N, int d, int causal, float scale, cudaStream_t stream,
+                            unsigned int* err, int num_sms);
+
 // The e4m3 forward (d = 128): q8, k8 [B*H][N][128] bytes, vt8 [B*H][128][v_pitch]
 // bytes, scales [B*H][ceil(N/128)] for Q and K and [B*H] for V.
 fa_status launch_fwd_fp8(const void* q8, const void* k8, const void* vt8, const float* q_scale, const float* k_scale,

@@ -77,6 +77,10 @@ DECODE = {
 
 DECODE_SPLITS = (8, 16, 32)
 
+# Block-sparse prefill: the Llama-3-8B-shaped problem (non-causal) under a
+# band + global + random block mask (block_mask_bigbird, 128-key blocks).
+SPARSE_PREFILL = Prefill("llama3_8b_prefill_bigbird", 2, 32, 4096, 128, False)
+
 
 @dataclass(frozen=True)
 class DecodeGQA:
@@ -171,6 +175,24 @@ def decode_gqa_inputs(B: int, Hq: int, Hkv: int, L: int, d: int, seed: int = 0, 
     else:
         seqlens = torch.full((B,), L, dtype=torch.int32)
     return q, k, v, seqlens.to(device)
+
+
+def block_mask_bigbird(T: int, heads: int = 1, window: int = 1, globals_: int = 1, random: int = 2,
+                       seed: int = 0) -> torch.Tensor:
+    """A seeded block mask [heads, T, T] (uint8) of the kind block-sparse
+    attention serves: a band of +-window blocks, the first `globals_` block rows
+    and columns, and `random` extra blocks per block row."""
+    g = torch.Generator().manual_seed(seed + 3)
+    m = torch.zeros((heads, T, T), dtype=torch.uint8)
+    idx = torch.arange(T)
+    band = (idx[:, None] - idx[None, :]).abs() <= window
+    m[:, band] = 1
+    m[:, :globals_, :] = 1
+    m[:, :, :globals_] = 1
+    for h in range(heads):
+        for i in range(T):
+            m[h, i, torch.randint(0, T, (random,), generator=g)] = 1
+    return m
 
 
 def row_subsets(B: int, H: int, N: int, n_rows: int, seed: int = 0):

@@ -71,6 +71,34 @@ fa_status fa_fwd(const void *q, const void *k, const void *v, void *o, float *ls
                  int causal, float scale, fa_stream_t stream);
 
 /*
+ * Block-sparse prefill forward.
+ *
+ * Defines: "FlashAttention 完全拆解（一）", block-sparse extension: given a
+ *   block-level mask, the S_ij blocks it removes are skipped (never loaded,
+ *   never multiplied), so IO and work shrink with the mask's density.
+ *
+ *   q, k, v, o, lse, B, H, N, d, causal, scale: as fa_fwd.
+ *   mask     DEVICE bytes [mask_heads][T][T], T = ceil(N / 128) (the kernel's
+ *            tile): key j is visible to query i when
+ *            mask[i / 128][j / 128] != 0 and, if causal, j <= i.
+ *   mask_heads  1 (one mask for every head) or H (head h uses mask h).
+ * A row with no visible key gets o = 0 and lse = -inf.
+ * Errors: as fa_fwd; FA_ERR_INVALID_ARG also for a NULL mask or another
+ *   mask_heads.
+ */
+fa_status fa_fwd_sparse(const void *q, const void *k, const void *v, const uint8_t *mask, int mask_heads, void *o,
+                        float *lse, int B, int H, int N, int d, int causal, float scale, fa_stream_t stream);
+
+/*
+ * Work plan of fa_fwd_sparse (host only; mask is a HOST pointer, same layout):
+ * pairs_allowed = (Q tile, K/V tile) block pairs the mask (and the causal
+ * rule) keeps, over all B*H heads; pairs_computed = pairs the kernel computes
+ * (each pair of Q tiles walks the union of their kept K/V tiles, at least one).
+ */
+fa_status fa_fwd_sparse_plan(const uint8_t *mask, int mask_heads, int B, int H, int N, int causal,
+                             long long *pairs_allowed, long long *pairs_computed);
+
+/*
  * FP8 (e4m3) block quantization for fa_fwd_fp8, with incoherent processing.
  *
  * Defines: "已有的几种大模型上下文支持情况" (cicada blog) §4.4 (FA-3's FP8

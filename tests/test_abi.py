@@ -217,3 +217,36 @@ def test_fp8_calls_reject_bad_arguments(lib):
     assert fwd(scale=0.0) == fa.FA_ERR_INVALID_ARG
     assert fwd(causal=5) == fa.FA_ERR_INVALID_ARG
     assert fwd(d=64) == fa.FA_ERR_UNSUPPORTED
+
+
+def test_sparse_plan_matches_the_pages_counts(lib):
+    """All-ones mask: every pair; under the causal rule T(T+1)/2 of T^2 (Lecture 5
+    notes §6.2); a mask keeping 1/s of the blocks keeps 1/s of the pairs (the
+    block-sparse extension: IO shrinks with the density)."""
+    import numpy as np
+
+    import exact_attention_29_gb300 as fa
+
+    T, N = 8, 8 * 128
+    ones = np.ones((T, T), np.uint8)
+    assert fa.fa_fwd_sparse_plan(ones, 2, 3, N) == (2 * 3 * T * T, 2 * 3 * T * T)
+    allowed, computed = fa.fa_fwd_sparse_plan(ones, 1, 1, N, causal=True)
+    assert allowed == T * (T + 1) // 2 == 36
+    # each pair of Q tiles walks the union of its K/V tiles: (i0 + 2) steps for both tiles
+    assert computed == sum(2 * (i0 + 2) for i0 in range(0, T, 2))
+    quarter = np.zeros((T, T), np.uint8)
+    quarter[:, ::4] = 1
+    allowed, _ = fa.fa_fwd_sparse_plan(quarter, 1, 1, N)
+    assert allowed * 4 == T * T
+
+
+def test_sparse_rejects_bad_arguments(lib):
+    import exact_attention_29_gb300 as fa
+
+    def sp(mask=16, mask_heads=1, H=2, d=128, scale=0.1):
+        return lib.fa_fwd_sparse(16, 16, 16, mask, mask_heads, 16, 16, 1, H, 300, d, 0, scale, None)
+
+    assert sp(mask=None) == fa.FA_ERR_INVALID_ARG
+    assert sp(mask_heads=3) == fa.FA_ERR_INVALID_ARG
+    assert sp(scale=-1.0) == fa.FA_ERR_INVALID_ARG
+    assert sp(d=96) == fa.FA_ERR_UNSUPPORTED
