@@ -74,6 +74,43 @@ fa_status current_device(int* dev_out) {
   return FA_OK;
 }
 
+// Workspaces come from a memory pool the library owns on each device, which
+// keeps up to kPoolKeepBytes mapped between calls (the default pool returns
+// its memory at every synchronisation, and mapping it again costs about
+// 0.1 ms per call). Allocation and release are stream-ordered.
+constexpr uint64_t kPoolKeepBytes = 1ull << 30;
+cudaMemPool_t g_pool[kMaxDevices] = {};
+
+fa_status ws_alloc(int dev, void** ptr, size_t bytes, cudaStream_t stream, const char* what) {
+  {
+    std::lock_guard<std::mutex> lock(g_mutex);
+    if (g_pool[dev] == nullptr) {
+      cudaMemPoolProps props = {};
+      props.allocType = cudaMemAllocationTypePinned;
+      props.handleTypes = cudaMemHandleTypeNone;
+      props.location.type = cudaMemLocationTypeDevice;
+      props.location.id = dev;
+      cudaMemPool_t pool = nullptr;
+      cudaError_t e = cudaMemPoolCreate(&pool, &props);
+      if (e == cudaSuccess) {
+        uint64_t keep = kPoolKeepBytes;
+        e = cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &keep);
+      }
+      if (e != cudaSuccess) {
+        set_error_text("cudaMemPoolCreate(workspace pool)", e);
+        return FA_ERR_CUDA;
+      }
+      g_pool[dev] = pool;
+    }
+  }
+  const cudaError_t e = cudaMallocFromPoolAsync(ptr, bytes, g_pool[dev], stream);
+  if (e != cudaSuccess) {
+    set_error_text(what, e);
+    return FA_ERR_CUDA;
+  }
+  return FA_OK;
+}
+
 }  // namespace
 
 void set_error_text(const char* what, cudaError_t err) {
@@ -211,8 +248,24 @@ fa_status fa_fwd_sparse(const void* q, const void* k, const void* v, const uint8
   if (st != FA_OK) return st;
   unsigned int* err = device_error_word();
   if (!err) return FA_ERR_CUDA;
-  return launch_fwd_sparse(q, k, v, mask, mask_heads, o, lse, B, H, N, d, causal, scale,
-                           reinterpret_cast<cudaStream_t>(stream), err, g_num_sms[dev]);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const size_t tiles = (static_cast<size_t>(N) + 127) / 128;
+  const size_t rows = static_cast<size_t>(mask_heads) * ((static_cast<size_t>(N) + 255) / 256);
+  void* ws = nullptr;
+  st = ws_alloc(dev, &ws, rows * tiles * sizeof(uint32_t) + rows * sizeof(int), s,
+                "workspace allocation (block-sparse step lists)");
+  if (st != FA_OK) return st;
+  cudaError_t e = cudaSuccess;
+  uint32_t* list = static_cast<uint32_t*>(ws);
+  int* cnt = reinterpret_cast<int*>(list + rows * tiles);
+  st = launch_fwd_sparse(q, k, v, mask, mask_heads, o, lse, B, H, N, d, causal, scale, list, cnt, s, err,
+                         g_num_sms[dev]);
+  e = cudaFreeAsync(ws, s);
+  if (st == FA_OK && e != cudaSuccess) {
+    set_error_text("cudaFreeAsync(block-sparse step lists)", e);
+    st = FA_ERR_CUDA;
+  }
+  return st;
 }
 
 fa_status fa_fwd_sparse_plan(const uint8_t* mask, int mask_heads, int B, int H, int N, int causal,
@@ -256,11 +309,10 @@ fa_status fa_quantize_fp8(const void* x, const float* signs, void* codes, float*
   if (st != FA_OK) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   void* ws = nullptr;
-  cudaError_t e = cudaMallocAsync(&ws, static_cast<size_t>(bh * tiles) * sizeof(float), s);
-  if (e != cudaSuccess) {
-    set_error_text("cudaMallocAsync(quantize workspace)", e);
-    return FA_ERR_CUDA;
-  }
+  st = ws_alloc(dev, &ws, static_cast<size_t>(bh * tiles) * sizeof(float), s,
+                "workspace allocation (quantize workspace)");
+  if (st != FA_OK) return st;
+  cudaError_t e = cudaSuccess;
   st = launch_quantize_fp8(x, signs, codes, scales, B, H, N, per_head, transpose, transpose ? v_pitch : 0,
                            static_cast<float*>(ws), s);
   e = cudaFreeAsync(ws, s);
@@ -311,11 +363,9 @@ fa_status fa_decode(const void* q, const void* k_cache, const void* v_cache, con
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const size_t parts = static_cast<size_t>(B) * H * num_splits;
   void* ws = nullptr;
-  cudaError_t e = cudaMallocAsync(&ws, parts * (d + 1) * sizeof(float), s);
-  if (e != cudaSuccess) {
-    set_error_text("cudaMallocAsync(decode workspace)", e);
-    return FA_ERR_CUDA;
-  }
+  st = ws_alloc(dev, &ws, parts * (d + 1) * sizeof(float), s, "workspace allocation (decode workspace)");
+  if (st != FA_OK) return st;
+  cudaError_t e = cudaSuccess;
   float* ws_o = static_cast<float*>(ws);
   float* ws_lse = ws_o + parts * d;
   st = launch_decode(q, k_cache, v_cache, seqlens, o, lse, B, H, L, d, num_splits, ws_o, ws_lse, s);
@@ -347,11 +397,9 @@ fa_status fa_decode_gqa(const void* q, const void* k_cache, const void* v_cache,
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const size_t parts = static_cast<size_t>(B) * Hq * num_splits;
   void* ws = nullptr;
-  cudaError_t e = cudaMallocAsync(&ws, parts * (d + 1) * sizeof(float), s);
-  if (e != cudaSuccess) {
-    set_error_text("cudaMallocAsync(decode workspace)", e);
-    return FA_ERR_CUDA;
-  }
+  st = ws_alloc(dev, &ws, parts * (d + 1) * sizeof(float), s, "workspace allocation (decode workspace)");
+  if (st != FA_OK) return st;
+  cudaError_t e = cudaSuccess;
   float* ws_o = static_cast<float*>(ws);
   float* ws_lse = ws_o + parts * d;
   st = launch_decode_gqa_split(q, k_cache, v_cache, seqlens, B, Hq, Hkv, L, d, num_splits, ws_o, ws_lse, s, err);
@@ -384,11 +432,9 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const size_t rows = static_cast<size_t>(bh) * N;
   void* ws = nullptr;
-  cudaError_t e = cudaMallocAsync(&ws, rows * (d + 1) * sizeof(float), s);
-  if (e != cudaSuccess) {
-    set_error_text("cudaMallocAsync(backward workspace)", e);
-    return FA_ERR_CUDA;
-  }
+  st = ws_alloc(dev, &ws, rows * (d + 1) * sizeof(float), s, "workspace allocation (backward workspace)");
+  if (st != FA_OK) return st;
+  cudaError_t e = cudaSuccess;
   float* dq_acc = static_cast<float*>(ws);
   float* delta = dq_acc + rows * d;
   st = launch_bwd(q, k, v, o, lse, dout, dq, dk, dv, B, H, N, d, causal, scale, dq_acc, delta, s, err);

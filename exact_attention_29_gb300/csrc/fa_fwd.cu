@@ -92,8 +92,12 @@ struct FwdParams {
   const float* sk;
   const float* sv;
   int tiles;
-  // block-sparse mode only: mask [mask_heads][tiles][tiles] bytes (nullptr: dense)
-  const uint8_t* mask;
+  // block-sparse mode only: per (mask head, Q-tile pair) the union of the K/V
+  // tiles its two Q tiles keep, as words (tile | allowed for Q tile 0 << 16 |
+  // allowed for Q tile 1 << 17), list[(mh * pairs + pair) * tiles + step], and
+  // the step counts cnt[mh * pairs + pair] (>= 1)
+  const uint32_t* list;
+  const int* cnt;
   int mask_heads;
   int H;
   int N;
@@ -144,51 +148,27 @@ __device__ __forceinline__ Smem carve(uint8_t* raw) {
   return s;
 }
 
-// Block-sparse mode ("FlashAttention 完全拆解（一）", block-sparse extension):
-// K/V tile j takes part for Q tile qi when the block mask allows it and, under
-// the causal mask, j <= qi (square tiles).
-__device__ __forceinline__ bool tile_allowed(const FwdParams& p, int bh, int qi, int j) {
-  if (p.causal && j > qi) return false;
-  const int mh = (p.mask_heads == 1) ? 0 : (bh % p.H);
-  return p.mask[(static_cast<size_t>(mh) * p.tiles + qi) * p.tiles + j] != 0;
-}
-
 // One work item: Q rows [q0, q0 + 256) of head bh; tile t visits n(t) K/V tiles.
-// Dense: tile t visits K/V tiles 0 .. n(t)-1. Block-sparse: both tiles walk the
-// union of their allowed K/V tiles in increasing order (a step that one tile's
-// mask removes is fully masked for that tile); an item whose union is empty
+// Dense: tile t visits K/V tiles 0 .. n(t)-1. Block-sparse ("FlashAttention
+// 完全拆解（一）", block-sparse extension): both tiles walk the union of the
+// K/V tiles their masks keep (sparse_list_kernel), a step that one tile's
+// mask removes being fully masked for that tile; an item whose union is empty
 // walks tile 0 fully masked, so its rows still get o = 0, lse = -inf.
 struct Item {
   int bh;
   int q0;
   int n0;
   int n1;
+  const uint32_t* list;  // block-sparse: this item's steps
   __device__ __forceinline__ int n(int t) const { return t ? n1 : n0; }
   __device__ __forceinline__ int n_max() const { return n0 > n1 ? n0 : n1; }
 };
 
-// Next K/V tile >= j in the item's union (p.tiles if none).
-__device__ __forceinline__ int union_next(const FwdParams& p, const Item& it, int j) {
-  const int qi0 = it.q0 / kBM;
-  const bool has1 = it.q0 + kBM < p.N;
-  for (; j < p.tiles; ++j)
-    if (tile_allowed(p, it.bh, qi0, j) || (has1 && tile_allowed(p, it.bh, qi0 + 1, j))) return j;
-  return p.tiles;
-}
-
-// K/V tile of the first step of an item.
+// K/V tile of step j, and whether Q tile t keeps it.
 template <bool SP>
-__device__ __forceinline__ int first_kv(const FwdParams& p, const Item& it) {
-  if constexpr (!SP) return 0;
-  const int j = union_next(p, it, 0);
-  return j < p.tiles ? j : 0;
-}
-
-// K/V tile of the step after the one on tile j.
-template <bool SP>
-__device__ __forceinline__ int next_kv(const FwdParams& p, const Item& it, int j) {
-  if constexpr (!SP) return j + 1;
-  return union_next(p, it, j + 1);
+__device__ __forceinline__ uint32_t step_word(const Item& it, int j) {
+  if constexpr (!SP) return static_cast<uint32_t>(j) | (3u << 16);
+  return __ldg(it.list + j);
 }
 
 // k-th item of this CTA (snake order over the heavy-first item list), or false.
@@ -205,10 +185,12 @@ __device__ __forceinline__ bool item_at(const FwdParams& p, int k, Item& it) {
   if constexpr (!SP) {
     it.n0 = fwd_kv_tiles(it.q0, p.N, kBN, p.causal);
     it.n1 = fwd_kv_tiles(it.q0 + kBM, p.N, kBN, p.causal);
+    it.list = nullptr;
   } else {
-    int nu = 0;
-    for (int j = union_next(p, it, 0); j < p.tiles; j = union_next(p, it, j + 1)) ++nu;
-    if (nu == 0) nu = 1;
+    const int mh = (p.mask_heads == 1) ? 0 : (it.bh % p.H);
+    const size_t row = static_cast<size_t>(mh) * p.num_pairs + pair;
+    const int nu = __ldg(p.cnt + row);
+    it.list = p.list + row * p.tiles;
     it.n0 = nu;
     it.n1 = (it.q0 + kBM < p.N) ? nu : 0;
   }
@@ -241,8 +223,10 @@ __device__ void load_role(const CUtensorMap* tm_q, const CUtensorMap* tm_k, cons
       ++q_cnt[t];
     }
     const int n_max = it.n_max();
-    int jt = first_kv<SP>(p, it);  // K/V tile of step j
-    for (int j = 0; j < n_max && ok; ++j, jt = next_kv<SP>(p, it, jt)) {
+    uint32_t next_word = step_word<SP>(it, 0);
+    for (int j = 0; j < n_max && ok; ++j) {
+      const int jt = static_cast<int>(next_word & 0xffffu);  // K/V tile of step j
+      if (j + 1 < n_max) next_word = step_word<SP>(it, j + 1);  // one step ahead
       for (int kind = 0; kind < 2; ++kind) {
         const uint32_t slot = ring % C::kStages;
         const uint32_t use = ring / C::kStages;
@@ -413,8 +397,11 @@ __device__ void softmax_role(const Smem& sm, uint32_t tmem, const FwdParams& p, 
     const int vis_end = p.causal ? min(q_row + 1, p.N) : p.N;  // keys [0, vis_end) are visible to this row
     float m_used = -INFINITY;  // base of every exponent so far (log2 domain, scaled)
     float l = 0.f;
-    int jt = first_kv<SP>(p, it);  // K/V tile of step j
-    for (int j = 0; j < nkv; ++j, jt = next_kv<SP>(p, it, jt)) {
+    uint32_t next_word = step_word<SP>(it, 0);
+    for (int j = 0; j < nkv; ++j) {
+      const uint32_t word = next_word;
+      if (j + 1 < nkv) next_word = step_word<SP>(it, j + 1);  // one step ahead
+      const int jt = static_cast<int>(word & 0xffffu);  // K/V tile of step j
       ok = bounded_wait(&sm.s_full[t], s_cnt & 1, sm.abort_flag, p.err, kSiteSFull);
       ++s_cnt;
       ok = __all_sync(kFull, ok);
@@ -431,7 +418,7 @@ __device__ void softmax_role(const Smem& sm, uint32_t tmem, const FwdParams& p, 
       // Pass 1: row maximum of the raw scores, 64 columns at a time (scale > 0,
       // so the maximum commutes with the scaling).
       // visible keys of this tile for this row (none when the block mask removes it)
-      const int lim = (SP && !tile_allowed(p, it.bh, it.q0 / kBM + t, jt)) ? 0 : vis_end - jt * kBN;
+      const int lim = ((word >> (16 + t)) & 1u) ? vis_end - jt * kBN : 0;
       float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
@@ -568,6 +555,39 @@ __device__ void softmax_role(const Smem& sm, uint32_t tmem, const FwdParams& p, 
   }
 }
 
+// Block-sparse step lists: one warp per (mask head, Q-tile pair) compacts, in
+// increasing order, the K/V tiles kept by either Q tile of the pair (the block
+// mask and, under the causal mask, j <= the Q tile's index).
+__global__ void __launch_bounds__(32) sparse_list_kernel(const uint8_t* __restrict__ mask, int tiles, int pairs,
+                                                         int causal, uint32_t* __restrict__ list,
+                                                         int* __restrict__ cnt) {
+  const int pair = blockIdx.x, mh = blockIdx.y, lane = threadIdx.x;
+  const uint8_t* mk = mask + static_cast<size_t>(mh) * tiles * tiles;
+  const int i0 = 2 * pair, i1 = 2 * pair + 1;
+  uint32_t* out = list + (static_cast<size_t>(mh) * pairs + pair) * tiles;
+  int n = 0;
+  for (int base = 0; base < tiles; base += 32) {
+    const int j = base + lane;
+    bool a0 = false, a1 = false;
+    if (j < tiles) {
+      a0 = mk[static_cast<size_t>(i0) * tiles + j] != 0 && (!causal || j <= i0);
+      a1 = i1 < tiles && mk[static_cast<size_t>(i1) * tiles + j] != 0 && (!causal || j <= i1);
+    }
+    const uint32_t keep = __ballot_sync(0xffffffffu, a0 || a1);
+    if (a0 || a1)
+      out[n + __popc(keep & ((1u << lane) - 1u))] =
+          static_cast<uint32_t>(j) | (a0 ? 1u << 16 : 0u) | (a1 ? 1u << 17 : 0u);
+    n += __popc(keep);
+  }
+  if (lane == 0) {
+    if (n == 0) {
+      out[0] = 0;  // tile 0, kept by neither: the rows get o = 0, lse = -inf
+      n = 1;
+    }
+    cnt[static_cast<size_t>(mh) * pairs + pair] = n;
+  }
+}
+
 template <int D, bool F8, bool SP>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -655,7 +675,7 @@ fa_status launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap
 template <int D>
 fa_status launch_bf16(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
                       int causal, float scale, cudaStream_t stream, unsigned int* err, int num_sms,
-                      const uint8_t* mask = nullptr, int mask_heads = 0) {
+                      const uint32_t* list = nullptr, const int* cnt = nullptr, int mask_heads = 0) {
   CUtensorMap tq, tk, tv;
   const uint64_t bh = static_cast<uint64_t>(B) * H;
   if (!encode_bf16_map(&tq, q, D, N, bh, kBM) || !encode_bf16_map(&tk, k, D, N, bh, kBN) ||
@@ -665,9 +685,10 @@ fa_status launch_bf16(const void* q, const void* k, const void* v, void* o, floa
   prm.o = static_cast<__nv_bfloat16*>(o);
   prm.lse = lse;
   prm.err = err;
-  prm.mask = mask;
+  prm.list = list;
+  prm.cnt = cnt;
   prm.mask_heads = mask_heads;
-  if (mask != nullptr) return launch<D, false, true>(tq, tk, tv, prm, B, H, N, causal, scale, stream, num_sms);
+  if (list != nullptr) return launch<D, false, true>(tq, tk, tv, prm, B, H, N, causal, scale, stream, num_sms);
   return launch<D, false, false>(tq, tk, tv, prm, B, H, N, causal, scale, stream, num_sms);
 }
 
@@ -681,13 +702,21 @@ fa_status launch_fwd(const void* q, const void* k, const void* v, void* o, float
 }
 
 fa_status launch_fwd_sparse(const void* q, const void* k, const void* v, const uint8_t* mask, int mask_heads, void* o,
-                            float* lse, int B, int H, int N, int d, int causal, float scale, cudaStream_t stream,
-                            unsigned int* err, int num_sms) {
+                            float* lse, int B, int H, int N, int d, int causal, float scale, uint32_t* list_ws,
+                            int* cnt_ws, cudaStream_t stream, unsigned int* err, int num_sms) {
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  const int tiles = (N + kBM - 1) / kBM;
+  const int pairs = (N + 2 * kBM - 1) / (2 * kBM);
+  sparse_list_kernel<<<dim3(static_cast<unsigned>(pairs), static_cast<unsigned>(mask_heads)), 32, 0, stream>>>(
+      mask, tiles, pairs, causal ? 1 : 0, list_ws, cnt_ws);
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) {
+    set_error_text("sparse_list_kernel launch", e);
+    return FA_ERR_CUDA;
+  }
   if (d == 128)
-    return launch_bf16<128>(q, k, v, o, lse, B, H, N, causal, scale, stream, err, num_sms, mask, mask_heads);
-  if (d == 64)
-    return launch_bf16<64>(q, k, v, o, lse, B, H, N, causal, scale, stream, err, num_sms, mask, mask_heads);
-  return FA_ERR_UNSUPPORTED;
+    return launch_bf16<128>(q, k, v, o, lse, B, H, N, causal, scale, stream, err, num_sms, list_ws, cnt_ws, mask_heads);
+  return launch_bf16<64>(q, k, v, o, lse, B, H, N, causal, scale, stream, err, num_sms, list_ws, cnt_ws, mask_heads);
 }
 
 fa_status launch_fwd_fp8(const void* q8, const void* k8, const void* vt8, const float* q_scale, const float* k_scale,

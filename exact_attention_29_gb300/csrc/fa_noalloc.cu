@@ -1,6 +1,6 @@
 // fa_decode_noalloc: Flash-Decoding without any device allocation.
 //
-// fa_decode takes its split-partials workspace from cudaMallocAsync on every
+// fa_decode takes its split-partials workspace from a stream-ordered pool on every
 // call. Some callers cannot allocate device memory at call time: a serving
 // engine that hands nearly all of HBM to its own KV-cache pool at start-up and
 // forbids allocation afterwards, or a latency-critical decode loop where an

@@ -32,14 +32,19 @@ def main():
     ap.add_argument("--iters", type=int, default=3)
     ap.add_argument("--batch", type=int, default=0)
     ap.add_argument("--splits", type=int, default=16)
+    ap.add_argument("--n", type=int, default=0, help="override the sequence length of a prefill workload")
     ap.add_argument("--bwd", action="store_true", help="time fa_bwd (after one fa_fwd) on a prefill workload")
     ap.add_argument("--fp8", action="store_true", help="time fa_fwd_fp8 on e4m3 inputs of a prefill workload")
+    ap.add_argument("--sparse", action="store_true",
+                    help="time fa_fwd_sparse under the band + global + random block mask (one per head)")
     args = ap.parse_args()
     build.build()
     dev = torch.device("cuda:0")
     stream = torch.cuda.current_stream(dev)
     if args.workload in wl.PREFILL:
         c = wl.PREFILL[args.workload]
+        if args.n:
+            c = wl.Prefill(c.name, c.B, c.H, args.n, c.d, c.causal)
         B = args.batch or c.B
         q, k, v = wl.prefill_inputs(B, c.H, c.N, c.d, seed=0, device=dev)
         o = torch.empty_like(q)
@@ -47,6 +52,14 @@ def main():
 
         def run():
             fa.fa_fwd(q, k, v, causal=c.causal, o=o, lse=lse, stream=stream)
+
+        if args.sparse:
+            mask = wl.block_mask_bigbird((c.N + 127) // 128, heads=c.H, seed=0)
+            allowed, computed = fa.fa_fwd_sparse_plan(mask, B, c.H, c.N, c.causal)
+            mask_d = mask.to(dev)
+
+            def run():
+                fa.fa_fwd_sparse(q, k, v, mask_d, causal=c.causal, o=o, lse=lse, stream=stream)
 
         if args.fp8:
             g = torch.Generator().manual_seed(1)
@@ -100,13 +113,19 @@ def main():
         from exact_attention_29_gb300 import perfmodel
 
         flops = (perfmodel.bwd_flops if args.bwd else perfmodel.fwd_flops)(B, c.H, c.N, c.d, c.causal)
-        extra = f" best {flops / min(times) / 1e9:.1f} TFLOP/s"
+        if args.sparse:
+            # the two products on the block pairs the mask keeps (4 * 128 * 128 * d each)
+            flops = 4.0 * 128 * 128 * c.d * allowed
+            extra = f" (kept {allowed} of {B * c.H * ((c.N + 127) // 128) ** 2} pairs, computed {computed})"
+        else:
+            extra = ""
+        extra = f" best {flops / min(times) / 1e9:.1f} TFLOP/s" + extra
     else:
         from exact_attention_29_gb300 import perfmodel
 
         kv = perfmodel.decode_kv_bytes(c.Hkv if hasattr(c, "Hkv") else c.H, c.d, sl.tolist())
         extra = f" best {kv / min(times) / 1e6:.0f} GB/s of K/V"
-    what = "bwd" if args.bwd else ("fwd_fp8" if args.fp8 else "fwd")
+    what = "bwd" if args.bwd else ("fwd_fp8" if args.fp8 else ("fwd_sparse" if args.sparse else "fwd"))
     print(f"{args.workload} {what if args.workload in wl.PREFILL else ''} B={B}: "
           + " ".join(f"{t:.3f}ms" for t in times) + extra)
 

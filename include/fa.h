@@ -12,6 +12,11 @@
  *              over shared K/V heads).
  *   fa_bwd     gradients of fa_fwd, recomputing P from the saved log-sum-exp.
  *
+ * Workspaces: calls that need scratch memory take it, ordered on `stream`,
+ * from a memory pool the library creates on each device (cudaMemPoolCreate)
+ * and give it back on the same stream before returning; the pool keeps up to
+ * 1 GiB mapped between calls, so repeated calls do not map memory again.
+ *
  * Conventions for every call:
  *   - Tensor arguments are DEVICE pointers (memory of the current CUDA device),
  *     owned by the caller, contiguous, row-major in the layout stated. The
@@ -83,6 +88,8 @@ fa_status fa_fwd(const void *q, const void *k, const void *v, void *o, float *ls
  *            mask[i / 128][j / 128] != 0 and, if causal, j <= i.
  *   mask_heads  1 (one mask for every head) or H (head h uses mask h).
  * A row with no visible key gets o = 0 and lse = -inf.
+ * Workspace: mask_heads*ceil(N/256)*(T+1)*4 bytes of stream-ordered device
+ *   memory (the per Q-tile-pair step lists a first small kernel builds).
  * Errors: as fa_fwd; FA_ERR_INVALID_ARG also for a NULL mask or another
  *   mask_heads.
  */
@@ -162,8 +169,8 @@ fa_status fa_fwd_fp8(const void *q8, const void *k8, const void *vt8, const floa
  *   lse      fp32 [B][H][N], natural log.
  *   dq, dk, dv  bf16 [B][H][N][d] outputs.
  *   B, H, N, d, causal, scale: as fa_fwd.
- * Workspace: B*H*N*(d+1)*4 bytes of stream-ordered device memory
- *   (cudaMallocAsync on `stream`, freed on it): the fp32 dQ accumulator and D.
+ * Workspace: B*H*N*(d+1)*4 bytes of stream-ordered device memory (the fp32
+ *   dQ accumulator and D), see "Workspaces" below.
  * Errors: as fa_fwd.
  */
 fa_status fa_bwd(const void *q, const void *k, const void *v, const void *o, const float *lse, const void *dout,
@@ -196,8 +203,8 @@ fa_status fa_bwd_plan(int N, int d, int block, int causal, long long *dq_atomic_
  *   d        64 or 128. scale is fixed at 1/sqrt(d).
  *   num_splits  1..64: keys of each sequence are cut into num_splits chunks of
  *            ceil(len/num_splits) rounded up to a multiple of 64 keys.
- * Workspace: the call allocates B*H*num_splits*(d+1)*4 bytes of stream-ordered
- *   device memory (cudaMallocAsync) and frees it on the same stream.
+ * Workspace: B*H*num_splits*(d+1)*4 bytes of stream-ordered device memory,
+ *   see "Workspaces" below.
  * Errors: as fa_fwd; FA_ERR_INVALID_ARG also for num_splits outside 1..64.
  */
 fa_status fa_decode(const void *q, const void *k_cache, const void *v_cache, const int32_t *seqlens, void *o,
@@ -237,7 +244,7 @@ fa_status fa_decode_gqa(const void *q, const void *k_cache, const void *v_cache,
  * Arguments, layouts, results and errors are those of fa_decode. The split
  * partials live in one fixed 16 MiB array of device memory owned by libfa.so
  * (every GPU that loads the library holds it until the process exits)
- * instead of a per-call cudaMallocAsync buffer; the call never allocates.
+ * instead of a per-call pool allocation; the call never allocates.
  *   - Limit: B * H * num_splits * (d + 1) <= 4,194,304 (fp32 values). Larger
  *     requests return FA_ERR_INVALID_ARG and fa_last_error_string() says why.
  *   - All calls on a device share the array, which keeps the last call's
