@@ -351,6 +351,27 @@ def run_gpu(args, world, rank, local):
     fp8_value = world * fwd_flops * fp8_steps / (fp8_ms * 1e-3) / 1e12
     del q8, k8, vt8
 
+    # block-sparse forward on the non-causal twin of the prefill under the band + global + random mask
+    sc = wl.SPARSE_PREFILL
+    smask = wl.block_mask_bigbird(sc.N // 128, heads=sc.H, seed=rank)
+    s_allowed, s_computed = fa.fa_fwd_sparse_plan(smask, sc.B, sc.H, sc.N, sc.causal)
+    smask_d = smask.to(dev)
+    for _ in range(3):
+        fa.fa_fwd_sparse(q, k, v, smask_d, causal=sc.causal, o=o8, lse=l8, stream=stream)
+    torch.cuda.synchronize(dev)
+    s0 = torch.cuda.Event(enable_timing=True)
+    s1 = torch.cuda.Event(enable_timing=True)
+    sparse_steps = max(1, min(args.steps, 100))
+    s0.record(stream)
+    for _ in range(sparse_steps):
+        fa.fa_fwd_sparse(q, k, v, smask_d, causal=sc.causal, o=o8, lse=l8, stream=stream)
+    s1.record(stream)
+    torch.cuda.synchronize(dev)
+    fa.fa_check_device_error(stream)
+    sparse_ms = reduce_max([s0.elapsed_time(s1)], world)[0]
+    sparse_flops = 4.0 * 128 * 128 * sc.d * s_allowed
+    sparse_value = world * sparse_flops * sparse_steps / (sparse_ms * 1e-3) / 1e12
+
     # GQA decode (64 query heads over 8 K/V heads), timed on its own after the step loop
     gc = wl.DECODE_GQA[GQA_NAME]
     gq, gkc, gvc, gsl = wl.decode_gqa_inputs(gc.B, gc.Hq, gc.Hkv, gc.L, gc.d, seed=rank, device=dev)
@@ -421,6 +442,28 @@ def run_gpu(args, world, rank, local):
     dec_roof["frac"] = dec_roof["achieved"] / dec_roof["peak"]
     dominant = dec_roof if dec_avg_ms >= fwd_avg_ms else fwd_roof
 
+    def leg_roof(bound, achieved, peak, unit, traffic_tag, kernel, peak_kind):
+        return {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit, "frac": achieved / peak,
+                "traffic": traffic.get(traffic_tag), "kernel": kernel, "peak_kind": peak_kind}
+
+    # GQA algorithmic bytes: K/V of the shared heads, plus q, o and lse of every query head
+    gqa_bytes = perfmodel.decode_algorithmic_bytes(gc.B, gc.Hq, gc.d, gsl.tolist()) - \
+        perfmodel.decode_kv_bytes(gc.Hq, gc.d, gsl.tolist()) + gqa_kv
+    leg_roofs = {
+        "backward": leg_roof("tensor", bwd_value / world, peaks["bf16_tflops"], "TFLOP/s",
+                             "bwd_kernel_128_llama3_8b_prefill", "bwd_kernel<128> (+ delta, convert)",
+                             "burst " + tag),
+        "fwd_fp8": leg_roof("tensor", fp8_value / world, 2 * peaks["bf16_tflops"], "TFLOP/s",
+                            "fwd_kernel_128_fp8_llama3_8b_prefill", "fwd_kernel<128, e4m3>",
+                            "2x burst bf16 " + tag + " (nominal e4m3/bf16 ratio)"),
+        "fwd_sparse": leg_roof("tensor", sparse_value / world, peaks["bf16_tflops"], "TFLOP/s",
+                               "fwd_kernel_128_sparse_llama3_8b_bigbird", "fwd_kernel<128, block-sparse>",
+                               "burst " + tag),
+        "decode_gqa": leg_roof("hbm", gqa_bytes / (gqa_ms / gqa_steps * 1e-3) / 1e9, peaks["hbm_gbs"], "GB/s",
+                               "decode_gqa_split_kernel_128_decode_gqa8_32k",
+                               "decode_gqa_split_kernel<128> + decode_merge_kernel<128>", "copy " + tag),
+    }
+
     c_tflops, c_dt, _, c_desc = cpu_oracle_sample(args.cpu_heads)
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
@@ -434,15 +477,21 @@ def run_gpu(args, world, rank, local):
         "decode": {"value": dec_gbs, "unit": "GB/s (KV read)", "frac_of_hbm": dec_gbs / peaks["hbm_gbs"],
                    "ms_per_step": dec_avg_ms},
         "prefill_ms_per_step": fwd_avg_ms,
-        "fwd_fp8": {"value": fp8_value, "unit": "TFLOP/s", "ms_per_call": fp8_ms / fp8_steps, "steps": fp8_steps,
+        "fwd_fp8": {"roofline": leg_roofs["fwd_fp8"], "value": fp8_value, "unit": "TFLOP/s", "ms_per_call": fp8_ms / fp8_steps, "steps": fp8_steps,
                     "frac_of_fp8_peak": fp8_value / world / (2 * peaks["bf16_tflops"]),
                     "peak_note": "fp8 peak taken as 2x the measured bf16 burst (the nominal dense ratio)",
                     "what": "fa_fwd_fp8 on e4m3 inputs of the prefill workload (quantized once, outside the timing)"},
-        "decode_gqa": {"value": gqa_gbs, "unit": "GB/s (KV read)", "ms_per_call": gqa_ms / gqa_steps,
+        "fwd_sparse": {"roofline": leg_roofs["fwd_sparse"], "value": sparse_value, "unit": "TFLOP/s (kept block pairs, 4*128*128*d each)",
+                       "ms_per_call": sparse_ms / sparse_steps, "steps": sparse_steps,
+                       "pairs_kept": s_allowed, "pairs_computed": s_computed,
+                       "pairs_all": sc.B * sc.H * (sc.N // 128) ** 2,
+                       "what": f"fa_fwd_sparse on {sc.name} (B{sc.B} H{sc.H} N{sc.N} d{sc.d}, non-causal) under the "
+                               "band + global + random block mask, one per head"},
+        "decode_gqa": {"roofline": leg_roofs["decode_gqa"], "value": gqa_gbs, "unit": "GB/s (KV read)", "ms_per_call": gqa_ms / gqa_steps,
                        "steps": gqa_steps, "frac_of_hbm": gqa_gbs / peaks["hbm_gbs"],
                        "what": f"fa_decode_gqa on {GQA_NAME} (B{gc.B} Hq{gc.Hq} Hkv{gc.Hkv} L{gc.L} d{gc.d}), "
                                f"{GQA_SPLITS} splits, timed after the step loop"},
-        "backward": {"value": bwd_value, "unit": "TFLOP/s (10 N^2 d per head, halved causal)",
+        "backward": {"roofline": leg_roofs["backward"], "value": bwd_value, "unit": "TFLOP/s (10 N^2 d per head, halved causal)",
                      "ms_per_call": bwd_ms / bwd_steps, "steps": bwd_steps,
                      "frac_of_bf16_peak": bwd_value / world / peaks["bf16_tflops"],
                      "what": "fa_bwd on the prefill workload (dQ zeroing, D, main kernel, dQ conversion), "
