@@ -223,10 +223,13 @@ __device__ void load_role(const CUtensorMap* tm_q, const CUtensorMap* tm_k, cons
       ++q_cnt[t];
     }
     const int n_max = it.n_max();
-    uint32_t next_word = step_word<SP>(it, 0);
+    uint32_t next_word = SP ? step_word<SP>(it, 0) : 0u;
     for (int j = 0; j < n_max && ok; ++j) {
-      const int jt = static_cast<int>(next_word & 0xffffu);  // K/V tile of step j
-      if (j + 1 < n_max) next_word = step_word<SP>(it, j + 1);  // one step ahead
+      int jt = j;  // K/V tile of step j
+      if constexpr (SP) {
+        jt = static_cast<int>(next_word & 0xffffu);
+        if (j + 1 < n_max) next_word = step_word<SP>(it, j + 1);  // one step ahead
+      }
       for (int kind = 0; kind < 2; ++kind) {
         const uint32_t slot = ring % C::kStages;
         const uint32_t use = ring / C::kStages;
@@ -397,11 +400,17 @@ __device__ void softmax_role(const Smem& sm, uint32_t tmem, const FwdParams& p, 
     const int vis_end = p.causal ? min(q_row + 1, p.N) : p.N;  // keys [0, vis_end) are visible to this row
     float m_used = -INFINITY;  // base of every exponent so far (log2 domain, scaled)
     float l = 0.f;
-    uint32_t next_word = step_word<SP>(it, 0);
+    uint32_t next_word = SP ? step_word<SP>(it, 0) : 0u;
     for (int j = 0; j < nkv; ++j) {
-      const uint32_t word = next_word;
-      if (j + 1 < nkv) next_word = step_word<SP>(it, j + 1);  // one step ahead
-      const int jt = static_cast<int>(word & 0xffffu);  // K/V tile of step j
+      // K/V tile of step j, and whether this Q tile keeps it
+      int jt = j;
+      bool keep = true;
+      if constexpr (SP) {
+        const uint32_t word = next_word;
+        if (j + 1 < nkv) next_word = step_word<SP>(it, j + 1);  // one step ahead
+        jt = static_cast<int>(word & 0xffffu);
+        keep = ((word >> (16 + t)) & 1u) != 0;
+      }
       ok = bounded_wait(&sm.s_full[t], s_cnt & 1, sm.abort_flag, p.err, kSiteSFull);
       ++s_cnt;
       ok = __all_sync(kFull, ok);
@@ -415,91 +424,147 @@ __device__ void softmax_role(const Smem& sm, uint32_t tmem, const FwdParams& p, 
         sl2x2 = f2_pack(sl2, sl2);
       }
 
-      // Pass 1: row maximum of the raw scores, 64 columns at a time (scale > 0,
-      // so the maximum commutes with the scaling).
       // visible keys of this tile for this row (none when the block mask removes it)
-      const int lim = ((word >> (16 + t)) & 1u) ? vis_end - jt * kBN : 0;
-      float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        uint32_t r[64];
-        tmem_ld_x64(s_tm + 64 * h, r);
+      const int lim = keep ? vis_end - jt * kBN : 0;
+      if constexpr (F8) {
+        // e4m3 inputs: one pass over the row. The 128 raw scores are loaded once, their
+        // maximum taken (scale > 0, so it commutes with the scaling), then
+        // p = 2^(s * scale * log2 e - m) in place, the row sum in packed pairs,
+        // and the P values packed in place and stored over the first columns of
+        // the S tile. O is rescaled afterwards, when the registers are free.
+        uint32_t r[128];
+        tmem_ld_x64(s_tm, *reinterpret_cast<uint32_t(*)[64]>(&r[0]));
+        tmem_ld_x64(s_tm + 64, *reinterpret_cast<uint32_t(*)[64]>(&r[64]));
         if (lim < kBN) {
-#pragma unroll
-          for (int c = 0; c < 64; ++c)
-            if (64 * h + c >= lim) r[c] = 0xff800000u;  // -inf
+  #pragma unroll
+          for (int c = 0; c < 128; ++c)
+            if (c >= lim) r[c] = 0xff800000u;  // -inf
         }
-#pragma unroll
-        for (int c = 0; c < 64; c += 8) {
-#pragma unroll
+        float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+  #pragma unroll
+        for (int c = 0; c < 128; c += 8) {
+  #pragma unroll
           for (int i = 0; i < 4; ++i)
             mx[i] = fmax3(mx[i], __uint_as_float(r[c + 2 * i]), __uint_as_float(r[c + 2 * i + 1]));
         }
-      }
-      const float m_tile = fmax3(fmaxf(mx[0], mx[1]), mx[2], mx[3]) * sl2;
+        const float m_tile = fmax3(fmaxf(mx[0], mx[1]), mx[2], mx[3]) * sl2;
 
-      const bool need = (m_used != -INFINITY) && (m_tile > m_used + kRescaleSlack);
-      if (__any_sync(kFull, need)) {
+        const bool need = (m_used != -INFINITY) && (m_tile > m_used + kRescaleSlack);
         const float alpha = need ? ex2_approx(m_used - m_tile) : 1.f;
-        if (need) {
-          l *= alpha;
-          m_used = m_tile;
-        }
-        const uint64_t alpha2 = f2_pack(alpha, alpha);
-#pragma unroll 1
-        for (int c = 0; c < D; c += 32) {
-          uint32_t r[32];
-          tmem_ld_x32(o_tm + c, r);
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            float lo, hi;
-            f2_unpack(f2_mul(f2_pack(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1])), alpha2), lo, hi);
-            r[2 * i] = __float_as_uint(lo);
-            r[2 * i + 1] = __float_as_uint(hi);
-          }
-          tmem_st_x32(o_tm + c, r);
-        }
-      }
-      if (m_used == -INFINITY) m_used = m_tile;  // first visible scores of this row
-      const float m_sub = (m_used == -INFINITY) ? 0.f : m_used;
+        if (need) m_used = m_tile;
+        if (m_used == -INFINITY) m_used = m_tile;  // first visible scores of this row
+        const float m_sub = (m_used == -INFINITY) ? 0.f : m_used;
 
-      // Pass 2: p = 2^(s * scale * log2 e - m), two at a time, row sum in
-      // packed pairs; the bf16 pairs of keys [64h, 64h + 64) go to P columns
-      // [32h, 32h + 32), which only hold scores this pass has already read.
-      const uint64_t negm2 = f2_pack(-m_sub, -m_sub);
-      uint64_t acc[4] = {0, 0, 0, 0};
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        uint32_t r[64];
-        tmem_ld_x64(s_tm + 64 * h, r);
-        if (lim < kBN) {
-#pragma unroll
-          for (int c = 0; c < 64; ++c)
-            if (64 * h + c >= lim) r[c] = 0xff800000u;
-        }
-        // x = s * scale_log2 - m in place, then 2^x in place (MUFU), then pack + sum
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
+        const uint64_t negm2 = f2_pack(-m_sub, -m_sub);
+        uint64_t acc[4] = {0, 0, 0, 0};
+  #pragma unroll
+        for (int i = 0; i < 64; ++i) {
           float x0, x1;
           f2_unpack(f2_fma(f2_pack(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1])), sl2x2, negm2), x0, x1);
-          r[2 * i] = __float_as_uint(ex2_approx(x0));
-          r[2 * i + 1] = __float_as_uint(ex2_approx(x1));
+          const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+          acc[i & 3] = f2_add(acc[i & 3], f2_pack(p0, p1));
+          r[2 * i] = __float_as_uint(p0);
+          r[2 * i + 1] = __float_as_uint(p1);
         }
-        if constexpr (F8) {
-          // e4m3 P: four keys per column, keys [64h, 64h + 64) to columns [16h, 16h + 16)
-          uint32_t pk[16];
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const float p0 = __uint_as_float(r[4 * i]), p1 = __uint_as_float(r[4 * i + 1]);
-            const float p2 = __uint_as_float(r[4 * i + 2]), p3 = __uint_as_float(r[4 * i + 3]);
-            acc[(2 * i) & 3] = f2_add(acc[(2 * i) & 3], f2_pack(p0, p1));
-            acc[(2 * i + 1) & 3] = f2_add(acc[(2 * i + 1) & 3], f2_pack(p2, p3));
-            pk[i] = pack_e4m3x2(p0, p1) | (pack_e4m3x2(p2, p3) << 16);
+        // e4m3 P: four keys per column, keys [0, 128) to columns [0, 32)
+  #pragma unroll
+        for (int i = 0; i < 32; ++i)
+          r[i] = pack_e4m3x2(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1])) |
+                 (pack_e4m3x2(__uint_as_float(r[4 * i + 2]), __uint_as_float(r[4 * i + 3])) << 16);
+        tmem_st_x32(s_tm, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
+        float s0, s1, s2, s3;
+        f2_unpack(f2_add(acc[0], acc[1]), s0, s1);
+        f2_unpack(f2_add(acc[2], acc[3]), s2, s3);
+        l = l * alpha + ((s0 + s1) + (s2 + s3));
+
+        if (__any_sync(kFull, need)) {
+          const uint64_t alpha2 = f2_pack(alpha, alpha);
+  #pragma unroll 1
+          for (int c = 0; c < D; c += 32) {
+            uint32_t o[32];
+            tmem_ld_x32(o_tm + c, o);
+  #pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              float lo, hi;
+              f2_unpack(f2_mul(f2_pack(__uint_as_float(o[2 * i]), __uint_as_float(o[2 * i + 1])), alpha2), lo, hi);
+              o[2 * i] = __float_as_uint(lo);
+              o[2 * i + 1] = __float_as_uint(hi);
+            }
+            tmem_st_x32(o_tm + c, o);
           }
-          tmem_st_x16(s_tm + 16 * h, pk);
-        } else {
+        }
+      } else {
+        // bf16 inputs, pass 1: row maximum of the raw scores, 64 columns at a time
+        // (scale > 0, so the maximum commutes with the scaling). Holding all 128
+        // scores at once, as the e4m3 path does, makes this instance spill.
+        float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+  #pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          uint32_t r[64];
+          tmem_ld_x64(s_tm + 64 * h, r);
+          if (lim < kBN) {
+  #pragma unroll
+            for (int c = 0; c < 64; ++c)
+              if (64 * h + c >= lim) r[c] = 0xff800000u;  // -inf
+          }
+  #pragma unroll
+          for (int c = 0; c < 64; c += 8) {
+  #pragma unroll
+            for (int i = 0; i < 4; ++i)
+              mx[i] = fmax3(mx[i], __uint_as_float(r[c + 2 * i]), __uint_as_float(r[c + 2 * i + 1]));
+          }
+        }
+        const float m_tile = fmax3(fmaxf(mx[0], mx[1]), mx[2], mx[3]) * sl2;
+
+        const bool need = (m_used != -INFINITY) && (m_tile > m_used + kRescaleSlack);
+        if (__any_sync(kFull, need)) {
+          const float alpha = need ? ex2_approx(m_used - m_tile) : 1.f;
+          if (need) {
+            l *= alpha;
+            m_used = m_tile;
+          }
+          const uint64_t alpha2 = f2_pack(alpha, alpha);
+  #pragma unroll 1
+          for (int c = 0; c < D; c += 32) {
+            uint32_t r[32];
+            tmem_ld_x32(o_tm + c, r);
+  #pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              float lo, hi;
+              f2_unpack(f2_mul(f2_pack(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1])), alpha2), lo, hi);
+              r[2 * i] = __float_as_uint(lo);
+              r[2 * i + 1] = __float_as_uint(hi);
+            }
+            tmem_st_x32(o_tm + c, r);
+          }
+        }
+        if (m_used == -INFINITY) m_used = m_tile;  // first visible scores of this row
+        const float m_sub = (m_used == -INFINITY) ? 0.f : m_used;
+
+        // Pass 2: p = 2^(s * scale * log2 e - m), two at a time, row sum in
+        // packed pairs; the bf16 pairs of keys [64h, 64h + 64) go to P columns
+        // [32h, 32h + 32), which only hold scores this pass has already read.
+        const uint64_t negm2 = f2_pack(-m_sub, -m_sub);
+        uint64_t acc[4] = {0, 0, 0, 0};
+  #pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          uint32_t r[64];
+          tmem_ld_x64(s_tm + 64 * h, r);
+          if (lim < kBN) {
+  #pragma unroll
+            for (int c = 0; c < 64; ++c)
+              if (64 * h + c >= lim) r[c] = 0xff800000u;
+          }
+          // x = s * scale_log2 - m in place, then 2^x in place (MUFU), then pack + sum
+  #pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            float x0, x1;
+            f2_unpack(f2_fma(f2_pack(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1])), sl2x2, negm2), x0, x1);
+            r[2 * i] = __float_as_uint(ex2_approx(x0));
+            r[2 * i + 1] = __float_as_uint(ex2_approx(x1));
+          }
           uint32_t pk[32];
-#pragma unroll
+  #pragma unroll
           for (int i = 0; i < 32; ++i) {
             const float p0 = __uint_as_float(r[2 * i]);
             const float p1 = __uint_as_float(r[2 * i + 1]);
@@ -508,11 +573,11 @@ __device__ void softmax_role(const Smem& sm, uint32_t tmem, const FwdParams& p, 
           }
           tmem_st_x32(s_tm + 32 * h, pk);
         }
+        float s0, s1, s2, s3;
+        f2_unpack(f2_add(acc[0], acc[1]), s0, s1);
+        f2_unpack(f2_add(acc[2], acc[3]), s2, s3);
+        l += (s0 + s1) + (s2 + s3);
       }
-      float s0, s1, s2, s3;
-      f2_unpack(f2_add(acc[0], acc[1]), s0, s1);
-      f2_unpack(f2_add(acc[2], acc[3]), s2, s3);
-      l += (s0 + s1) + (s2 + s3);
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(&sm.p_full[t]);
