@@ -483,24 +483,32 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const int q0 = (i_first + it) * 128;
         const int nq = min(128, p.N - q0);
         float* dst = p.dq_acc + (head_rows + q0) * D + dcol;
-#pragma unroll 1
-        for (int c = 0; c < 128; c += 32) {
-          uint32_t r[32];
-          tmem_ld_x32(dq_tm + c, r);
-          if (c == 96) {
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bars[kBarDqEmpty]);
-          }
-          if (c + 32 <= nq) {
+        // 32 queries (TMEM columns c0 ..) of this dQ column: scaled reductions
+        auto add32 = [&](const uint32_t (&r)[32], int c0) {
+          if (c0 + 32 <= nq) {
 #pragma unroll
-            for (int e = 0; e < 32; ++e) red_add_f32(dst + static_cast<size_t>(c + e) * D, __uint_as_float(r[e]) * p.scale);
+            for (int e = 0; e < 32; ++e) red_add_f32(dst + static_cast<size_t>(c0 + e) * D, __uint_as_float(r[e]) * p.scale);
           } else {
 #pragma unroll
             for (int e = 0; e < 32; ++e)
-              if (c + e < nq) red_add_f32(dst + static_cast<size_t>(c + e) * D, __uint_as_float(r[e]) * p.scale);
+              if (c0 + e < nq) red_add_f32(dst + static_cast<size_t>(c0 + e) * D, __uint_as_float(r[e]) * p.scale);
           }
-        }
+        };
+        // Three slices in registers, the first one added, the fourth loaded into
+        // its registers: the TMEM columns go back to the next dP after 32
+        // reductions instead of 96.
+        uint32_t r0[32], r1[32], r2[32];
+        tmem_ld_x32(dq_tm, r0);
+        tmem_ld_x32(dq_tm + 32, r1);
+        tmem_ld_x32(dq_tm + 64, r2);
+        add32(r0, 0);
+        tmem_ld_x32(dq_tm + 96, r0);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars[kBarDqEmpty]);
+        add32(r1, 32);
+        add32(r2, 64);
+        add32(r0, 96);
       }
     } else {
       static_assert(D == 64, "one 64-column pair");
