@@ -450,6 +450,29 @@ def run_gpu(args, world, rank, local):
     e2e_value = world * fwd_flops * e2e_steps / (e2e_ms * 1e-3) / 1e12
     h2d = sum(t.numel() * t.element_size() for t in (q, k, v))
     d2h = o.numel() * o.element_size() + lse.numel() * lse.element_size()
+
+    # the host link alone: one step's uploads and downloads, at the same time on
+    # the same two streams, no kernel; the pipeline above cannot beat this
+    def link_step():
+        with torch.cuda.stream(s_in):
+            for dst, src in zip(bufs_in[0], (hq, hk, hv)):
+                dst.copy_(src, non_blocking=True)
+        with torch.cuda.stream(s_out):
+            hosts_out[0][0].copy_(bufs_out[0][0], non_blocking=True)
+            hosts_out[0][1].copy_(bufs_out[0][1], non_blocking=True)
+
+    link_step()
+    torch.cuda.synchronize(dev)
+    l0 = torch.cuda.Event(enable_timing=True)
+    l1 = torch.cuda.Event(enable_timing=True)
+    l0.record(s_in)
+    s_out.wait_stream(s_in)
+    for _ in range(5):
+        link_step()
+    s_out.wait_stream(s_in)
+    l1.record(s_out)
+    torch.cuda.synchronize(dev)
+    link_ms = l0.elapsed_time(l1) / 5
     del bufs_in, bufs_out
 
     if rank != 0:
@@ -532,9 +555,13 @@ def run_gpu(args, world, rank, local):
                          "sample": c_desc, "seconds": c_dt},
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "steps": e2e_steps,
+                "link": {"ms_per_step": link_ms, "h2d_gbs": h2d / (link_ms * 1e-3) / 1e9,
+                         "frac": link_ms / (e2e_ms / e2e_steps),
+                         "what": "one step's uploads and downloads alone (same streams, no kernel): the host "
+                                 "link's bound on a step; frac = that time / the pipelined step time"},
                 "what": "prefill through fa_fwd with pinned host buffers; every step uploads q/k/v and downloads "
                         "o/lse inside the timed region, double-buffered over three streams (upload of step s+1 "
-                        "and download of step s-1 overlap step s; the upload of 201 MB at ~190 GB/s bounds a step)"},
+                        "and download of step s-1 overlap step s)"},
         "gpu_launches": 3 * args.steps,
         "clocks": clocks,
     }
