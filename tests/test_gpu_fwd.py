@@ -154,6 +154,27 @@ def test_output_buffers_and_stream():
     compare(o, lse, o_ref, lse_ref, "side stream")
 
 
+@pytest.mark.parametrize("d", [64, 128])
+def test_output_16_byte_aligned_only(d):
+    """An output that is 16- but not 32-byte aligned takes the 16-byte store
+    path of the epilogue; both paths write the same bits."""
+    import exact_attention_29_gb300 as fa
+
+    q, k, v = wl.prefill_inputs(2, 3, 333, d, seed=10)
+    q, k, v = q.cuda(), k.cuda(), v.cuda()
+    o_a = torch.empty_like(q)
+    flat = torch.empty(q.numel() + 8, dtype=q.dtype, device="cuda")
+    o_b = flat[8:].view(q.shape)  # 16 bytes past a 256-byte boundary
+    assert o_a.data_ptr() % 32 == 0 and o_b.data_ptr() % 32 == 16
+    lse = torch.empty((2, 3, 333), device="cuda")
+    fa.fa_fwd(q, k, v, causal=True, o=o_a, lse=lse)
+    fa.fa_fwd(q, k, v, causal=True, o=o_b, lse=lse)
+    fa.fa_check_device_error()
+    assert torch.equal(o_a, o_b)
+    o_ref, lse_ref = oracle.attention(q.cpu(), k.cpu(), v.cpu(), True, d ** -0.5)
+    compare(o_b, lse, o_ref, lse_ref, "16-byte aligned output")
+
+
 def test_python_binding_rejects_bad_tensors():
     import exact_attention_29_gb300 as fa
 
