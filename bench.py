@@ -196,6 +196,18 @@ def cpu_oracle_sample(n_heads: int, seed: int = 0):
     return flops / dt / 1e12, dt, flops, f"{len(heads)} of {c.B * c.H} heads of {PREFILL_NAME}, all {c.N} rows each"
 
 
+def arm_config(world: int, splits: int) -> dict:
+    """The workload both arms report (the same dict in the GPU and the reference line)."""
+    from exact_attention_29_gb300 import workloads as wl
+
+    pc, dc = wl.PREFILL[PREFILL_NAME], wl.DECODE[DECODE_NAME]
+    return {"workload": f"{PREFILL_NAME} + {DECODE_NAME}",
+            "prefill": {"B": pc.B, "H": pc.H, "N": pc.N, "d": pc.d, "causal": pc.causal},
+            "decode": {"B": dc.B, "H": dc.H, "L": dc.L, "d": dc.d, "num_splits": splits},
+            "l2": "inputs larger than L2 (prefill q/k/v/o 268 MB, decode KV 8.6 GB); no flush",
+            "parallelism": f"replicas x{world}"}
+
+
 def run_reference(args, world, rank):
     """The reference arm: the fp64 CPU oracle, as it stands, on the host cores."""
     if rank != 0:
@@ -215,8 +227,8 @@ def run_reference(args, world, rank):
         "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / max(1, args.steps),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": PREFILL_NAME, "B": 2, "H": 32, "N": 4096, "d": 128, "causal": True,
-                   "sample_per_step": desc},
+        "config": arm_config(world, args.splits),
+        "sample_per_step": desc + " (value is the prefill's TFLOP/s, as in the GPU line; the oracle times no decode)",
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": _cores(), "kind": "oracle", "sample": desc},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -521,11 +533,7 @@ def run_gpu(args, world, rank, local):
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": max(3, args.warmup), "ms_per_step": total_ms / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": f"{PREFILL_NAME} + {DECODE_NAME}",
-                   "prefill": {"B": pc.B, "H": pc.H, "N": pc.N, "d": pc.d, "causal": pc.causal},
-                   "decode": {"B": dc.B, "H": dc.H, "L": dc.L, "d": dc.d, "num_splits": splits},
-                   "l2": "inputs larger than L2 (prefill q/k/v/o 268 MB, decode KV 8.6 GB); no flush",
-                   "parallelism": f"replicas x{world}"},
+        "config": arm_config(world, splits),
         "decode": {"value": dec_gbs, "unit": "GB/s (KV read)", "frac_of_hbm": dec_gbs / peaks["hbm_gbs"],
                    "ms_per_step": dec_avg_ms},
         "prefill_ms_per_step": fwd_avg_ms,
