@@ -28,10 +28,14 @@
 //               registers), bf16 P^T to TMEM (for dV), then dS = P (dP - D) to
 //               TMEM (for dK) and, transposed, to shared memory (for dQ = dS K,
 //               whose A operand must be query-major).
-//   warps 0-3   read the dQ share out of TMEM, stage it in shared memory and
-//               add scale * dQ to the fp32 accumulator with bulk tensor
-//               reductions (the atomic additions of §7.4, done by the TMA unit
-//               on whole 128-byte rows).
+//   warps 0-3   read the dQ share out of TMEM and add scale * dQ to the fp32
+//               accumulator (the atomic additions of §7.4). d = 128: the share
+//               is dQ^T (d on the lanes); each warp loads three 32-column
+//               slices, adds the first with coalesced red.global.add (one
+//               128-byte segment of a dQ row per instruction), loads the fourth
+//               and returns the columns to the next dP before adding the rest.
+//               d = 64: the share is dQ; it is staged in shared memory and added
+//               with bulk tensor reductions on whole 128-byte rows.
 // Every wait is bounded (fa_common.cuh).
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>

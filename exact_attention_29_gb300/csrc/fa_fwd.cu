@@ -277,6 +277,12 @@ __device__ __forceinline__ void pv_product(uint32_t o_tmem, uint32_t p_tmem, uin
     issue_pv<D>(o_tmem, p_tmem, v_smem, accumulate);
 }
 
+// At every step tile 0's products are issued before tile 1's. The buffer
+// releases depend on it: a K or V tile both read is released by tile 1 (its
+// last reader) once tile 1's product on it completes, which then implies tile
+// 0's. Issuing a tile's products as soon as they are ready, or starting tile 0
+// on its next item early, also breaks the lock-step the two tiles need to share
+// a K/V ring two steps deep.
 template <int D, bool F8, bool SP>
 __device__ void mma_role(const Smem& sm, uint32_t tmem, const FwdParams& p) {
   using C = Cfg<D, F8>;
