@@ -106,6 +106,7 @@ struct FwdParams {
   int num_items;   // BH * num_pairs
   int causal;
   int o_v8;          // o is 32-byte aligned: the epilogue writes 32-byte pieces of a row
+  int swap_tiles;    // dense causal items: tile 0 takes the pair's second 128 rows
   float scale_log2;  // scale * log2(e)
 };
 
@@ -158,10 +159,12 @@ __device__ __forceinline__ Smem carve(uint8_t* raw) {
 struct Item {
   int bh;
   int q0;
+  int r0, r1;  // first query row of tile 0 and of tile 1
   int n0;
   int n1;
   const uint32_t* list;  // block-sparse: this item's steps
   __device__ __forceinline__ int n(int t) const { return t ? n1 : n0; }
+  __device__ __forceinline__ int row(int t) const { return t ? r1 : r0; }
   __device__ __forceinline__ int n_max() const { return n0 > n1 ? n0 : n1; }
 };
 
@@ -184,13 +187,19 @@ __device__ __forceinline__ bool item_at(const FwdParams& p, int k, Item& it) {
   const int pair = p.causal ? (p.num_pairs - 1 - rank) : rank;
   it.q0 = pair * 2 * kBM;
   if constexpr (!SP) {
-    it.n0 = fwd_kv_tiles(it.q0, p.N, kBN, p.causal);
-    it.n1 = fwd_kv_tiles(it.q0 + kBM, p.N, kBN, p.causal);
+    // swap_tiles: tile 0 takes the later rows (under the causal mask one K/V
+    // step more), so tile 1's epilogue runs while tile 0 takes that step alone
+    it.r0 = p.swap_tiles ? it.q0 + kBM : it.q0;
+    it.r1 = p.swap_tiles ? it.q0 : it.q0 + kBM;
+    it.n0 = fwd_kv_tiles(it.r0, p.N, kBN, p.causal);
+    it.n1 = fwd_kv_tiles(it.r1, p.N, kBN, p.causal);
     it.list = nullptr;
   } else {
     const int mh = (p.mask_heads == 1) ? 0 : (it.bh % p.H);
     const size_t row = static_cast<size_t>(mh) * p.num_pairs + pair;
     const int nu = __ldg(p.cnt + row);
+    it.r0 = it.q0;
+    it.r1 = it.q0 + kBM;
     it.list = p.list + row * p.tiles;
     it.n0 = nu;
     it.n1 = (it.q0 + kBM < p.N) ? nu : 0;
@@ -220,7 +229,7 @@ __device__ void load_role(const CUtensorMap* tm_q, const CUtensorMap* tm_k, cons
       mbar_arrive_expect_tx(&sm.q_full[t], C::kTileBytes);
 #pragma unroll
       for (int c = 0; c < C::kChunks; ++c)
-        tma_load_3d(sm.q[t] + c * kChunkBytes, tm_q, &sm.q_full[t], c * 64, it.q0 + t * kBM, it.bh);
+        tma_load_3d(sm.q[t] + c * kChunkBytes, tm_q, &sm.q_full[t], c * 64, it.row(t), it.bh);
       ++q_cnt[t];
     }
     const int n_max = it.n_max();
@@ -403,7 +412,7 @@ __device__ void softmax_role(const Smem& sm, uint32_t tmem, const FwdParams& p, 
     ring_next += 2 * it.n_max();
     const int nkv = it.n(t);
     if (nkv == 0) continue;
-    const int q_row = it.q0 + t * kBM + row;
+    const int q_row = it.row(t) + row;
     const int vis_end = p.causal ? min(q_row + 1, p.N) : p.N;  // keys [0, vis_end) are visible to this row
     float m_used = -INFINITY;  // base of every exponent so far (log2 domain, scaled)
     float l = 0.f;
@@ -427,7 +436,7 @@ __device__ void softmax_role(const Smem& sm, uint32_t tmem, const FwdParams& p, 
       if constexpr (F8) {
         // block-wise scales of the e4m3 inputs: Q tile and K tile j of this head
         const size_t sb = static_cast<size_t>(it.bh) * p.tiles;
-        sl2 = p.scale_log2 * __ldg(p.sq + sb + (it.q0 / kBM) + t) * __ldg(p.sk + sb + jt);
+        sl2 = p.scale_log2 * __ldg(p.sq + sb + it.row(t) / kBM) * __ldg(p.sk + sb + jt);
         sl2x2 = f2_pack(sl2, sl2);
       }
 
@@ -733,6 +742,10 @@ fa_status launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap
   prm.num_items = static_cast<int>(items);
   prm.causal = causal ? 1 : 0;
   prm.o_v8 = (reinterpret_cast<uintptr_t>(prm.o) & 31u) == 0 ? 1 : 0;
+  // Which tile of a causal pair goes first is a matter of how the two tiles'
+  // chains overlap at item boundaries; measured per instance: the swapped order
+  // is faster for e4m3 (+2 %) and d = 64 (+6 %), slower for bf16 d = 128 (-1 to -3 %).
+  prm.swap_tiles = (!SP && causal && (F8 || D == 64)) ? 1 : 0;
   prm.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   prm.tiles = (N + kBM - 1) / kBM;
   prm.H = H;
