@@ -33,6 +33,8 @@ if ROOT not in sys.path:
 
 METRIC = "attn fwd TFLOP/s (% of GB300 BF16 peak); decode KV-read GB/s (% of HBM)"
 PREFILL_NAME = "llama3_8b_prefill"
+NOMINAL_BF16_TFLOPS = 2250.0  # GB300 dense bf16 tensor peak (nominal)
+NOMINAL_HBM_GBS = 7900.0      # GB300 HBM3e bandwidth (nominal)
 DECODE_NAME = "decode_32k"
 DEFAULT_SPLITS = 16
 GQA_NAME = "decode_gqa8_32k"
@@ -500,10 +502,13 @@ def run_gpu(args, world, rank, local):
                 "unit": "TFLOP/s", "traffic": traffic.get("fwd_kernel_128_llama3_8b_prefill"),
                 "kernel": "fwd_kernel<128>", "peak_kind": ("sustained " if long_region else "burst ") + tag}
     fwd_roof["frac"] = fwd_roof["achieved"] / fwd_roof["peak"]
+    # the metric's own denominators: GB300 nominal dense bf16 and HBM3e bandwidth
+    fwd_roof["frac_of_nominal"] = fwd_roof["achieved"] / NOMINAL_BF16_TFLOPS
     dec_roof = {"bound": "hbm", "achieved": dec_bytes / (dec_avg_ms * 1e-3) / 1e9, "peak": peaks["hbm_gbs"],
                 "unit": "GB/s", "traffic": traffic.get("decode_split_kernel_128_decode_32k"),
                 "kernel": "decode_split_kernel<128> + decode_merge_kernel<128>", "peak_kind": "copy " + tag}
     dec_roof["frac"] = dec_roof["achieved"] / dec_roof["peak"]
+    dec_roof["frac_of_nominal"] = dec_roof["achieved"] / NOMINAL_HBM_GBS
     dominant = dec_roof if dec_avg_ms >= fwd_avg_ms else fwd_roof
 
     def leg_roof(bound, achieved, peak, unit, traffic_tag, kernel, peak_kind):
