@@ -6,6 +6,7 @@ Importing the package does not load the library; the first call does, and
 fails loudly if it has not been built.
 """
 from ._lib import (  # noqa: F401
+    FA_ERR_CHECK,
     FA_ERR_CUDA,
     FA_ERR_INVALID_ARG,
     FA_ERR_TIMEOUT,

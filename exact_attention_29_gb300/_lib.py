@@ -15,13 +15,15 @@ import threading
 import torch
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_PKG, "libfa.so")
+# FA_LIBRARY may name another build of the library (libfa_debug.so: FA_DEBUG protocol checks)
+LIB_PATH = os.environ.get("FA_LIBRARY") or os.path.join(_PKG, "libfa.so")
 
 FA_OK = 0
 FA_ERR_INVALID_ARG = 1
 FA_ERR_UNSUPPORTED = 2
 FA_ERR_CUDA = 3
 FA_ERR_TIMEOUT = 4
+FA_ERR_CHECK = 5
 
 _lib = None
 _lock = threading.Lock()
@@ -367,7 +369,7 @@ def fa_check_device_error(stream=None) -> int:
     lib = load_library()
     site = ctypes.c_int(0)
     st = lib.fa_check_device_error(_stream_handle(stream), ctypes.byref(site))
-    if st == FA_ERR_TIMEOUT:
+    if st in (FA_ERR_TIMEOUT, FA_ERR_CHECK):
         err = FaError(st, f"fa_check_device_error (site {site.value})")
         err.site = site.value
         raise err

@@ -3,6 +3,12 @@
 Each translation unit compiles in its own nvcc process, in parallel, into
 ``_build/``; the objects are then linked into ``exact_attention_29_gb300/libfa.so``.
 Run ``python -m exact_attention_29_gb300.build`` or call ``build()``.
+
+``build(debug=True)`` (``--debug``) makes ``libfa_debug.so`` instead, compiled
+with FA_DEBUG: at the end of each pipelined kernel the roles' protocol counts
+(items, ring positions, barrier phases, tiles) are compared, and a mismatch is
+reported by fa_check_device_error as FA_ERR_CHECK. The binding loads it when
+FA_LIBRARY names it.
 """
 from __future__ import annotations
 
@@ -16,6 +22,8 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(PKG, "csrc")
 OUT_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libfa.so")
+DEBUG_OUT_DIR = os.path.join(PKG, "_build_debug")
+DEBUG_LIB = os.path.join(PKG, "libfa_debug.so")
 SOURCES = ["fa_api.cu", "fa_fwd.cu", "fa_bwd.cu", "fa_decode.cu", "fa_decode_gqa.cu", "fa_quant.cu", "fa_selftest.cu", "fa_noalloc.cu"]
 HEADERS = ["sm103.cuh", "fa_common.cuh", "fa_mma.cuh", "fa_internal.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -37,16 +45,20 @@ def _newest_input() -> float:
     return max(os.path.getmtime(p) for p in paths)
 
 
-def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) -> str:
-    """Compile every translation unit and link libfa.so; returns its path."""
-    if not force and os.path.exists(LIB) and os.path.getmtime(LIB) >= _newest_input():
-        return LIB
+def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False, debug: bool = False) -> str:
+    """Compile every translation unit and link libfa.so (libfa_debug.so with
+    debug=True); returns its path."""
+    lib_path, out_dir = (DEBUG_LIB, DEBUG_OUT_DIR) if debug else (LIB, OUT_DIR)
+    if not force and os.path.exists(lib_path) and os.path.getmtime(lib_path) >= _newest_input():
+        return lib_path
     nvcc = _nvcc()
-    os.makedirs(OUT_DIR, exist_ok=True)
+    os.makedirs(out_dir, exist_ok=True)
     extra = ["-Xptxas", "-v"] if ptxas_info else []
+    if debug:
+        extra = extra + ["-DFA_DEBUG"]
 
     def compile_one(src: str) -> str:
-        obj = os.path.join(OUT_DIR, src.replace(".cu", ".o"))
+        obj = os.path.join(out_dir, src.replace(".cu", ".o"))
         cmd = [nvcc] + NVCC_FLAGS + extra + ["-c", os.path.join(CSRC, src), "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
@@ -57,14 +69,15 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
 
     with cf.ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
         objs = list(ex.map(compile_one, SOURCES))
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib_path + f".tmp{os.getpid()}"
     cmd = [nvcc] + ARCH + ["-shared", "-o", tmp] + objs
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib_path)
+    return lib_path
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose=True, ptxas_info="--ptxas" in sys.argv))
+    print(build(force="--force" in sys.argv, verbose=True, ptxas_info="--ptxas" in sys.argv,
+                debug="--debug" in sys.argv))

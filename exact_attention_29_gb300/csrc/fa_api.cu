@@ -205,6 +205,7 @@ const char* fa_status_string(fa_status status) {
     case FA_ERR_UNSUPPORTED: return "FA_ERR_UNSUPPORTED: unsupported head dimension or device";
     case FA_ERR_CUDA: return "FA_ERR_CUDA: a CUDA call failed";
     case FA_ERR_TIMEOUT: return "FA_ERR_TIMEOUT: a bounded wait inside a kernel ran out";
+    case FA_ERR_CHECK: return "FA_ERR_CHECK: a kernel's roles disagreed on their protocol counts (FA_DEBUG build)";
   }
   return "unknown fa_status";
 }
@@ -478,7 +479,8 @@ fa_status fa_check_device_error(fa_stream_t stream, int* site) {
     return FA_ERR_CUDA;
   }
   if (site) *site = static_cast<int>(host[1]);
-  return (host[0] & kErrTimeout) ? FA_ERR_TIMEOUT : FA_OK;
+  if (host[0] & kErrTimeout) return FA_ERR_TIMEOUT;
+  return (host[0] & kErrCheck) ? FA_ERR_CHECK : FA_OK;
 }
 
 fa_status fa_fwd_plan(int N, int block, int causal, long long* pairs_total, long long* pairs_computed) {

@@ -164,6 +164,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(base + C::kBarOff);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(&bars[kNumBars]);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(&bars[kNumBars + 1]);
+  // [4] Q tiles completed by the load, MMA, P/dS and read-out roles (FA_DEBUG builds)
+  uint32_t* dbg = reinterpret_cast<uint32_t*>(&bars[kNumBars + 2]);
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
@@ -195,6 +197,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     mbar_init(&bars[kBarAcc], 1);
     mbar_init(&bars[kBarStageFree], 4);
     *abort_flag = 0;
+    for (int i = 0; i < 4; ++i) dbg[i] = 0;
     fence_barrier_init();
   }
   if (warp == 0) {
@@ -220,7 +223,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
     }
     bool ok = true;
-    for (int it = 0; it < n_it && ok; ++it) {
+    int it = 0;
+    for (; it < n_it && ok; ++it) {
       const int b = it & 1;
       const int q0 = (i_first + it) * 128;
       if (it >= 2) ok = bounded_wait(&bars[kBarQEmpty + b], ((it - 2) >> 1) & 1, abort_flag, p.err, kSiteQEmpty);
@@ -253,6 +257,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         ++do_cnt;
       }
     }
+#ifdef FA_DEBUG
+    if (lane == 0) dbg[0] = static_cast<uint32_t>(it);
+#endif
     // every copy issued must land before the CTA exits
     if (lane == 0) {
       bounded_wait(&bars[kBarKv], 0, nullptr, p.err, kSiteDrain);
@@ -277,7 +284,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         issue_qk<D>(dp_tm, smem_u32(sv), smem_u32(sdo));
         umma_commit(&bars[kBarDp]);
       }
-      for (int it = 0; it < n_it && ok; ++it) {
+      int it = 0;
+      for (; it < n_it && ok; ++it) {
         const int b = it & 1;
         const bool more = it + 1 < n_it;
         // dV += P^T dO as soon as P^T is in TMEM
@@ -315,6 +323,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           umma_commit(&bars[kBarDp]);
         }
       }
+#ifdef FA_DEBUG
+      dbg[1] = static_cast<uint32_t>(it);
+#endif
       // completes once every product above has; the epilogue reads dK and dV after it
       umma_commit(&bars[kBarAcc]);
       bounded_wait(&bars[kBarAcc], 0, nullptr, p.err, kSiteDrain);
@@ -331,7 +342,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const uint32_t dp_tm = tmem + lane_base + C::kColDp + 64 * half;
     uint8_t* ds_row = sds + half * kChunkBytes + row * 128;
     bool ok = true;
-    for (int it = 0; it < n_it; ++it) {
+    int it = 0;
+    for (; it < n_it; ++it) {
       const int b = it & 1;
       const int i = i_first + it;
       ok = bounded_wait(&bars[kBarS], it & 1, abort_flag, p.err, kSiteSFull) &&
@@ -437,6 +449,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars[kBarDs]);
     }
+#ifdef FA_DEBUG
+    if (warp == 4 && lane == 0) dbg[2] = static_cast<uint32_t>(it);
+#endif
     // dK = scale * acc and dV = acc for this key row, columns of this half of d
     if (ok) ok = bounded_wait(&bars[kBarAcc], 0, abort_flag, p.err, kSiteOFull);
     if (__all_sync(kFull, ok)) {
@@ -480,7 +495,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const uint32_t dq_tm = tmem + (static_cast<uint32_t>(warp * 32) << 16) + C::kColDp;
     if constexpr (D == 128) {
       const int dcol = warp * 32 + lane;
-      for (int it = 0; it < n_it; ++it) {
+      int it = 0;
+      for (; it < n_it; ++it) {
         const bool ok = bounded_wait(&bars[kBarDq], it & 1, abort_flag, p.err, kSitePFull);
         if (!__all_sync(kFull, ok)) break;
         tc_fence_after();
@@ -514,10 +530,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         add32(r2, 64);
         add32(r0, 96);
       }
+#ifdef FA_DEBUG
+      if (warp == 0 && lane == 0) dbg[3] = static_cast<uint32_t>(it);
+#endif
     } else {
       static_assert(D == 64, "one 64-column pair");
       if (lane == 0 && warp == 0) tma_prefetch_desc(&tm_dq);
-      for (int it = 0; it < n_it; ++it) {
+      int it = 0;
+      for (; it < n_it; ++it) {
         const bool ok = bounded_wait(&bars[kBarDq], it & 1, abort_flag, p.err, kSitePFull);
         if (!__all_sync(kFull, ok)) break;
         tc_fence_after();
@@ -550,11 +570,21 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
       // the additions must be complete before the CTA exits
       if (lane == 0) bulk_wait_group<0>();
+#ifdef FA_DEBUG
+      if (warp == 0 && lane == 0) dbg[3] = static_cast<uint32_t>(it);
+#endif
     }
   }
 
   tc_fence_before();
   __syncthreads();
+#ifdef FA_DEBUG
+  // protocol check: every role completed every Q tile of this K/V tile
+  if (tid == 0 && *abort_flag == 0) {
+    const uint32_t n = static_cast<uint32_t>(n_it);
+    if (dbg[0] != n || dbg[1] != n || dbg[2] != n || dbg[3] != n) record_check(p.err, kSiteCheckBwd);
+  }
+#endif
   if (warp == 0) {
     __syncwarp();
     tc_fence_after();

@@ -13,9 +13,11 @@ namespace fa {
 // legitimately longer than a few microseconds.
 constexpr uint64_t kWaitTimeoutNs = 2000000000ull;
 
-// Device error word: err[0] holds flags (bit 0 = a bounded wait ran out),
-// err[1] the site code of the first wait that ran out.
+// Device error word: err[0] holds flags (bit 0 = a bounded wait ran out,
+// bit 1 = a protocol check of an FA_DEBUG build failed), err[1] the site code
+// of the first wait or check that failed.
 constexpr unsigned int kErrTimeout = 1u;
+constexpr unsigned int kErrCheck = 2u;
 
 // Site codes (which wait ran out), reported by fa_check_device_error.
 enum WaitSite : int {
@@ -28,11 +30,19 @@ enum WaitSite : int {
   kSiteDrain = 7,
   kSiteQEmpty = 8,
   kSiteOEmpty = 9,
+  kSiteCheckFwd = 20,  // FA_DEBUG: the forward's roles disagree (items, ring, phases)
+  kSiteCheckBwd = 21,  // FA_DEBUG: the backward's roles completed different tile counts
+  kSiteCheckGqa = 22,  // FA_DEBUG: the GQA decode's roles disagree on the tiles of a split
   kSiteSelftest = 100,
 };
 
 __device__ __forceinline__ void record_timeout(unsigned int* err, int site) {
   atomicOr(&err[0], kErrTimeout);
+  atomicCAS(&err[1], 0u, static_cast<unsigned int>(site));
+}
+
+__device__ __forceinline__ void record_check(unsigned int* err, int site) {
+  atomicOr(&err[0], kErrCheck);
   atomicCAS(&err[1], 0u, static_cast<unsigned int>(site));
 }
 

@@ -107,6 +107,8 @@ __global__ void __launch_bounds__(kGqaThreads, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(base + C::kBarOff);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(&bars[kGNumBars]);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(&bars[kGNumBars + 1]);
+  // [4] tiles copied, O products issued, tiles of each softmax warpgroup (FA_DEBUG builds)
+  uint32_t* dbg = reinterpret_cast<uint32_t*>(&bars[kGNumBars + 2]);
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
@@ -147,6 +149,7 @@ __global__ void __launch_bounds__(kGqaThreads, 1)
     mbar_init(&bars[kGQ], 1);
     mbar_init(&bars[kGDone], 1);
     *abort_flag = 0;
+    for (int i = 0; i < 4; ++i) dbg[i] = 0;
     fence_barrier_init();
   }
   if (warp == 0) {
@@ -184,6 +187,9 @@ __global__ void __launch_bounds__(kGqaThreads, 1)
       // every copy issued must land before the CTA exits
       for (int t = (issued > C::kStages ? issued - C::kStages : 0); t < issued; ++t)
         bounded_wait(&bars[kGFull + t % C::kStages], (t / C::kStages) & 1, nullptr, p.err, kSiteDrain);
+#ifdef FA_DEBUG
+      dbg[0] = static_cast<uint32_t>(issued);
+#endif
     }
   } else if (warp == kIssueWarp) {
     // ------------------------------------------------------------ products
@@ -253,6 +259,9 @@ __global__ void __launch_bounds__(kGqaThreads, 1)
           ok = false;
         }
       }
+#ifdef FA_DEBUG
+      dbg[1] = static_cast<uint32_t>(next_o);
+#endif
       // every product must complete before TMEM is freed
       umma_commit(&bars[kGDone]);
       bounded_wait(&bars[kGDone], 0, nullptr, p.err, kSiteDrain);
@@ -387,6 +396,9 @@ __global__ void __launch_bounds__(kGqaThreads, 1)
     }
     // this group's last product, then its summary (m, l) per query
     if (ok && tiles_done > 0) ok = bounded_wait(&bars[kGO + wg], (tiles_done - 1) & 1, abort_flag, p.err, kSiteOFull);
+#ifdef FA_DEBUG
+    if (wt == 0) dbg[2 + wg] = static_cast<uint32_t>(tiles_done);
+#endif
     if (seg == 0) {
       s_l[qi] = l_run;
       s_m[qi] = m_run;
@@ -419,6 +431,14 @@ __global__ void __launch_bounds__(kGqaThreads, 1)
 
   tc_fence_before();
   __syncthreads();
+#ifdef FA_DEBUG
+  // protocol check: every tile of the split was copied once, multiplied once
+  // into O, and taken by one softmax warpgroup
+  if (tid == 0 && *abort_flag == 0) {
+    const uint32_t n = static_cast<uint32_t>(n_tiles);
+    if (dbg[0] != n || dbg[1] != n || dbg[2] + dbg[3] != n) record_check(p.err, kSiteCheckGqa);
+  }
+#endif
   if (warp == 0) {
     __syncwarp();
     tc_fence_after();

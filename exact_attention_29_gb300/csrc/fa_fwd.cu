@@ -80,7 +80,8 @@ struct Cfg {
   static constexpr int kBarOff = kRingOff + kStages * kTileBytes;
   // q_full, q_empty, s_full, p_full, o_full, o_empty (2 each), kv_full, kv_empty, mma_done
   static constexpr int kNumBars = 12 + 2 * kStages + 1;
-  static constexpr int kSmemBytes = kBarOff + kNumBars * 8 + 16 + 1024;  // + slack to align to 1 KB
+  // + TMEM slot, abort flag, 16 protocol counters (FA_DEBUG), slack to align to 1 KB
+  static constexpr int kSmemBytes = kBarOff + kNumBars * 8 + 16 + 64 + 1024;
 };
 
 struct FwdParams {
@@ -124,6 +125,7 @@ struct Smem {
   uint64_t* mma_done;  // [1]   every product done (teardown)
   uint32_t* tmem_slot;
   volatile int* abort_flag;
+  uint32_t* dbg;       // [16] per-role protocol counters, compared at the end (FA_DEBUG builds)
 };
 
 template <int D, bool F8>
@@ -147,6 +149,7 @@ __device__ __forceinline__ Smem carve(uint8_t* raw) {
   s.mma_done = s.kv_empty + C::kStages;
   s.tmem_slot = reinterpret_cast<uint32_t*>(s.mma_done + 1);
   s.abort_flag = reinterpret_cast<volatile int*>(s.tmem_slot + 1);
+  s.dbg = reinterpret_cast<uint32_t*>(s.tmem_slot + 4);
   return s;
 }
 
@@ -267,6 +270,11 @@ __device__ void load_role(const CUtensorMap* tm_q, const CUtensorMap* tm_k, cons
     bounded_wait(&sm.kv_full[r % C::kStages], (r / C::kStages) & 1, nullptr, p.err, kSiteDrain);
   for (int t = 0; t < 2; ++t)
     if (q_cnt[t] > 0) bounded_wait(&sm.q_full[t], (q_cnt[t] - 1) & 1, nullptr, p.err, kSiteDrain);
+#ifdef FA_DEBUG
+  sm.dbg[0] = ring;
+  sm.dbg[1] = q_cnt[0];
+  sm.dbg[2] = q_cnt[1];
+#endif
 }
 
 // ---------------------------------------------------------------- MMA issuer (one thread)
@@ -368,6 +376,14 @@ __device__ void mma_role(const Smem& sm, uint32_t tmem, const FwdParams& p) {
   // Teardown: every product issued so far must finish before TMEM is freed.
   umma_commit(sm.mma_done);
   bounded_wait(sm.mma_done, 0, nullptr, p.err, kSiteDrain);
+#ifdef FA_DEBUG
+  sm.dbg[3] = ring;
+  for (int t = 0; t < 2; ++t) {
+    sm.dbg[4 + t] = q_cnt[t];
+    sm.dbg[6 + t] = p_cnt[t];
+    sm.dbg[8 + t] = o_cnt[t];
+  }
+#endif
 }
 
 // The tile whose products read K_j and V_j last (tile 1 unless it stops earlier).
@@ -641,6 +657,13 @@ __device__ void softmax_role(const Smem& sm, uint32_t tmem, const FwdParams& p, 
       p.lse[static_cast<size_t>(it.bh) * p.N + q_row] = (l > 0.f) ? (m_used + log2f(l)) * kLn2 : -INFINITY;
     }
   }
+#ifdef FA_DEBUG
+  if (releaser) {
+    sm.dbg[10 + t] = ring_next;
+    sm.dbg[12 + t] = s_cnt;
+    sm.dbg[14 + t] = o_cnt;
+  }
+#endif
 }
 
 // Block-sparse step lists: one warp per (mask head, Q-tile pair) compacts, in
@@ -701,6 +724,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(sm.mma_done, 1);
     *sm.abort_flag = 0;
+    for (int i = 0; i < 16; ++i) sm.dbg[i] = 0;
     fence_barrier_init();
   }
   if (warp == kMmaWarp) {
@@ -722,6 +746,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
+#ifdef FA_DEBUG
+  // Protocol check: the roles walked the same items (ring positions), and per
+  // tile the MMA consumed one Q per item and one P per S the softmax saw, and
+  // produced one O per item the epilogue read.
+  if (threadIdx.x == 0 && *sm.abort_flag == 0) {
+    const uint32_t* d = sm.dbg;
+    bool good = d[0] == d[3] && d[0] == d[10] && d[0] == d[11];
+    for (int t = 0; t < 2; ++t)
+      good = good && d[1 + t] == d[4 + t] && d[4 + t] == d[8 + t] && d[6 + t] == d[12 + t] && d[8 + t] == d[14 + t];
+    if (!good) record_check(p.err, kSiteCheckFwd);
+  }
+#endif
   if (warp == kMmaWarp) {
     __syncwarp();
     tc_fence_after();

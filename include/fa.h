@@ -47,7 +47,8 @@ typedef enum {
   FA_ERR_INVALID_ARG = 1,  /* null pointer, non-positive size, misaligned pointer, bad scale */
   FA_ERR_UNSUPPORTED = 2,  /* valid but not implemented here (head dim other than 64 or 128, no sm_103 device) */
   FA_ERR_CUDA = 3,         /* a CUDA runtime or driver call failed; see fa_last_error_string() */
-  FA_ERR_TIMEOUT = 4       /* a kernel's bounded wait ran out; the kernel stopped and its outputs are undefined */
+  FA_ERR_TIMEOUT = 4,      /* a kernel's bounded wait ran out; the kernel stopped and its outputs are undefined */
+  FA_ERR_CHECK = 5         /* a libfa_debug.so build only: a kernel's roles disagreed on their protocol counts */
 } fa_status;
 
 /*
@@ -267,9 +268,11 @@ const char *fa_last_error_string(void);
 /*
  * Synchronise `stream`, then read and clear the device error word of the
  * current device. Returns FA_ERR_TIMEOUT if a kernel recorded that one of its
- * bounded waits ran out since the last check, FA_ERR_CUDA if the stream
- * reports an error, FA_OK otherwise. `site`, if not NULL, receives the code of
- * the first wait that ran out (0 if none).
+ * bounded waits ran out since the last check, FA_ERR_CHECK if (in a library
+ * built with FA_DEBUG) a kernel's end-of-kernel protocol check failed: its
+ * roles did not walk the same items, ring positions and barrier phases.
+ * FA_ERR_CUDA if the stream reports an error, FA_OK otherwise. `site`, if not
+ * NULL, receives the code of the first wait or check that failed (0 if none).
  */
 fa_status fa_check_device_error(fa_stream_t stream, int *site);
 

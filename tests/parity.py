@@ -3,6 +3,8 @@
 Tolerances (bf16 inputs, fp32 accumulation, bf16 output): max |dO| <= 2e-2,
 mean |dO| <= 2e-3 over all compared elements, |dLSE| <= 1e-3 absolute.
 """
+import os
+
 import numpy as np
 import pytest
 
@@ -11,16 +13,43 @@ MEAN_ABS_O = 2e-3
 MAX_ABS_LSE = 1e-3
 
 
+# Every comparison is recorded (test, case, error figures, pass or fail); the
+# session writes them as JSON lines to $FA_PARITY_REPORT when it is set.
+RECORDS = []
+CURRENT_TEST = {"id": ""}
+
+
+def record(kind, what, ok, **figures):
+    RECORDS.append({"test": CURRENT_TEST["id"], "kind": kind, "case": what, "pass": bool(ok),
+                    **{k: float(v) for k, v in figures.items()}})
+
+
+def write_report():
+    path = os.environ.get("FA_PARITY_REPORT")
+    if not path or not RECORDS:
+        return
+    import json
+
+    with open(path, "w") as f:
+        for r in RECORDS:
+            f.write(json.dumps(r) + "\n")
+
+
 def compare(o_gpu, lse_gpu, o_ref, lse_ref, what=""):
     """o_gpu / lse_gpu: torch tensors (any device); o_ref / lse_ref: fp64 numpy."""
     o = o_gpu.float().cpu().numpy().astype(np.float64)
     lse = lse_gpu.float().cpu().numpy().astype(np.float64)
     assert o.shape == o_ref.shape and lse.shape == lse_ref.shape, what
-    assert np.all(np.isfinite(o)) and np.all(np.isfinite(lse)), f"{what}: non-finite output"
+    finite = bool(np.all(np.isfinite(o)) and np.all(np.isfinite(lse)))
+    if not finite:
+        record("forward", what, False, elements=o.size)
+    assert finite, f"{what}: non-finite output"
     do = np.abs(o - o_ref)
     dl = np.abs(lse - lse_ref)
     msg = f"{what}: max|dO|={do.max():.3e} mean|dO|={do.mean():.3e} max|dLSE|={dl.max():.3e}"
-    assert do.max() <= MAX_ABS_O and do.mean() <= MEAN_ABS_O and dl.max() <= MAX_ABS_LSE, msg
+    ok = do.max() <= MAX_ABS_O and do.mean() <= MEAN_ABS_O and dl.max() <= MAX_ABS_LSE
+    record("forward", what, ok, max_abs_dO=do.max(), mean_abs_dO=do.mean(), max_abs_dLSE=dl.max(), elements=o.size)
+    assert ok, msg
     return do.max(), do.mean(), dl.max()
 
 
@@ -61,6 +90,8 @@ def compare_grads(got, ref, what=""):
         mx, mn = err.max() / max(np.abs(r).max(), 1e-30), err.mean() / max(np.abs(r).mean(), 1e-30)
         ok = (err.max() <= GRAD_MAX_REL * np.abs(r).max() + GRAD_ATOL
               and err.mean() <= GRAD_MEAN_REL * np.abs(r).mean() + GRAD_ATOL)
+        record("backward", f"{what} {name}", ok, max_abs=err.max(), ref_max_abs=np.abs(r).max(),
+               mean_abs=err.mean(), ref_mean_abs=np.abs(r).mean(), elements=err.size)
         assert ok, f"{what} {name}: max|err| {err.max():.3e} (rel {mx:.3e}) mean|err| {err.mean():.3e} (rel {mn:.3e})"
         out.append((mx, mn))
     return out

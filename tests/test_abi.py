@@ -42,7 +42,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_status_strings(lib):
-    for code in range(5):
+    for code in range(6):
         s = lib.fa_status_string(code)
         assert s and s.startswith(b"FA_")
     assert lib.fa_status_string(99) == b"unknown fa_status"

@@ -17,7 +17,7 @@ import torch
 import oracle
 from oracle import fp8 as ofp8
 from exact_attention_29_gb300 import workloads as wl
-from parity import require_gpu
+from parity import record, require_gpu
 
 pytestmark = pytest.mark.gpu
 
@@ -61,7 +61,9 @@ def _compare(o, lse, o_ref, lse_ref, what):
     assert np.all(np.isfinite(o)) and np.all(np.isfinite(lse)), what
     do, dl = np.abs(o - o_ref), np.abs(lse - lse_ref)
     msg = f"{what}: max|dO|={do.max():.3e} mean|dO|={do.mean():.3e} max|dLSE|={dl.max():.3e}"
-    assert do.max() <= FP8_MAX_ABS_O and do.mean() <= FP8_MEAN_ABS_O and dl.max() <= FP8_MAX_ABS_LSE, msg
+    ok = do.max() <= FP8_MAX_ABS_O and do.mean() <= FP8_MEAN_ABS_O and dl.max() <= FP8_MAX_ABS_LSE
+    record("forward e4m3", what, ok, max_abs_dO=do.max(), mean_abs_dO=do.mean(), max_abs_dLSE=dl.max(), elements=o.size)
+    assert ok, msg
 
 
 @pytest.mark.parametrize("causal", [False, True])
