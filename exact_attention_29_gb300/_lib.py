@@ -100,6 +100,16 @@ def _require(t: torch.Tensor, name: str, dtype, ndim: int) -> None:
         raise ValueError(f"{name} must be contiguous")
 
 
+def _require_shape(t: torch.Tensor, name: str, dtype, shape, device) -> None:
+    """t must be a contiguous CUDA tensor of `dtype` and exactly `shape` on `device`
+    (the library is given raw pointers, so a wrong extent would be written past)."""
+    _require(t, name, dtype, len(shape))
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    if t.device != device:
+        raise ValueError(f"{name} must be on {device}, got {t.device}")
+
+
 def fa_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = False, scale: float | None = None,
            o: torch.Tensor | None = None, lse: torch.Tensor | None = None, stream=None):
     """Fused prefill attention. q, k, v: bf16 [B, H, N, d] on the GPU.
@@ -119,10 +129,9 @@ def fa_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = Fal
         o = torch.empty_like(q)
     if lse is None:
         lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
-    _require(o, "o", torch.bfloat16, 4)
-    _require(lse, "lse", torch.float32, 3)
-    if o.shape != q.shape or lse.shape != (B, H, N):
-        raise ValueError("o must match q and lse must be [B, H, N]")
+    for t, n in ((k, "k"), (v, "v"), (o, "o")):
+        _require_shape(t, n, torch.bfloat16, q.shape, q.device)
+    _require_shape(lse, "lse", torch.float32, (B, H, N), q.device)
     st = lib.fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), B, H, N, d,
                     1 if causal else 0, float(scale), _stream_handle(stream))
     _check(st, "fa_fwd")
@@ -137,9 +146,10 @@ def fa_fwd_sparse(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, mask: torch
     Returns (o bf16 [B, H, N, d], lse fp32 [B, H, N]).
     """
     lib = load_library()
-    for t, n in ((q, "q"), (k, "k"), (v, "v")):
-        _require(t, n, torch.bfloat16, 4)
+    _require(q, "q", torch.bfloat16, 4)
     B, H, N, d = q.shape
+    for t, n in ((k, "k"), (v, "v")):
+        _require_shape(t, n, torch.bfloat16, q.shape, q.device)
     T = (N + 127) // 128
     mask = mask.to(torch.uint8).contiguous()
     if mask.dim() == 2:
@@ -152,6 +162,8 @@ def fa_fwd_sparse(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, mask: torch
         o = torch.empty_like(q)
     if lse is None:
         lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    _require_shape(o, "o", torch.bfloat16, q.shape, q.device)
+    _require_shape(lse, "lse", torch.float32, (B, H, N), q.device)
     st = lib.fa_fwd_sparse(q.data_ptr(), k.data_ptr(), v.data_ptr(), mask.data_ptr(), mask.shape[0], o.data_ptr(),
                            lse.data_ptr(), B, H, N, d, 1 if causal else 0, float(scale), _stream_handle(stream))
     _check(st, "fa_fwd_sparse")
@@ -216,12 +228,20 @@ def fa_fwd_fp8(q8: torch.Tensor, k8: torch.Tensor, vt8: torch.Tensor, q_scale: t
     B, H, N, d = q8.shape
     if k8.shape != q8.shape or vt8.shape[:3] != (B, H, d) or vt8.shape[3] < N:
         raise ValueError("shapes must be q8, k8 [B,H,N,d] and vt8 [B,H,d,pitch >= N]")
+    if k8.device != q8.device or vt8.device != q8.device:
+        raise ValueError("q8, k8 and vt8 must be on the same device")
+    tiles = (N + 127) // 128
+    _require_shape(q_scale, "q_scale", torch.float32, (B, H, tiles), q8.device)
+    _require_shape(k_scale, "k_scale", torch.float32, (B, H, tiles), q8.device)
+    _require_shape(v_scale, "v_scale", torch.float32, (B, H), q8.device)
     if scale is None:
         scale = d ** -0.5
     if o is None:
         o = torch.empty((B, H, N, d), dtype=torch.bfloat16, device=q8.device)
     if lse is None:
         lse = torch.empty((B, H, N), dtype=torch.float32, device=q8.device)
+    _require_shape(o, "o", torch.bfloat16, (B, H, N, d), q8.device)
+    _require_shape(lse, "lse", torch.float32, (B, H, N), q8.device)
     st = lib.fa_fwd_fp8(q8.data_ptr(), k8.data_ptr(), vt8.data_ptr(), q_scale.data_ptr(), k_scale.data_ptr(),
                         v_scale.data_ptr(), o.data_ptr(), lse.data_ptr(), B, H, N, d, 1 if causal else 0,
                         float(scale), vt8.shape[3], _stream_handle(stream))
@@ -287,8 +307,8 @@ def fa_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, seq
         o = torch.empty_like(q)
     if lse is None:
         lse = torch.empty((B, H), dtype=torch.float32, device=q.device)
-    _require(o, "o", torch.bfloat16, 3)
-    _require(lse, "lse", torch.float32, 2)
+    _require_shape(o, "o", torch.bfloat16, (B, H, d), q.device)
+    _require_shape(lse, "lse", torch.float32, (B, H), q.device)
     st = lib.fa_decode(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), seqlens.data_ptr(), o.data_ptr(),
                        lse.data_ptr(), B, H, L, d, int(num_splits), _stream_handle(stream))
     _check(st, "fa_decode")
@@ -318,8 +338,8 @@ def fa_decode_gqa(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
         o = torch.empty_like(q)
     if lse is None:
         lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
-    _require(o, "o", torch.bfloat16, 3)
-    _require(lse, "lse", torch.float32, 2)
+    _require_shape(o, "o", torch.bfloat16, (B, Hq, d), q.device)
+    _require_shape(lse, "lse", torch.float32, (B, Hq), q.device)
     st = lib.fa_decode_gqa(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), seqlens.data_ptr(), o.data_ptr(),
                            lse.data_ptr(), B, Hq, Hkv, L, d, int(num_splits), _stream_handle(stream))
     _check(st, "fa_decode_gqa")
@@ -353,8 +373,8 @@ def fa_decode_noalloc(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Ten
         o = torch.empty_like(q)
     if lse is None:
         lse = torch.empty((B, H), dtype=torch.float32, device=q.device)
-    _require(o, "o", torch.bfloat16, 3)
-    _require(lse, "lse", torch.float32, 2)
+    _require_shape(o, "o", torch.bfloat16, (B, H, d), q.device)
+    _require_shape(lse, "lse", torch.float32, (B, H), q.device)
     st = lib.fa_decode_noalloc(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), seqlens.data_ptr(),
                                o.data_ptr(), lse.data_ptr(), B, H, L, d, int(num_splits), _stream_handle(stream))
     if st == FA_ERR_INVALID_ARG:

@@ -175,6 +175,42 @@ def test_output_16_byte_aligned_only(d):
     compare(o_b, lse, o_ref, lse_ref, "16-byte aligned output")
 
 
+def test_bindings_reject_wrong_shapes_before_any_launch():
+    """The library takes raw pointers; the binding refuses tensors whose extent
+    or device does not match (caller-provided outputs and scales included)."""
+    import exact_attention_29_gb300 as fa
+
+    q = torch.zeros((1, 2, 200, 64), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(ValueError):
+        fa.fa_fwd(q, q, q, o=torch.empty((1, 2, 100, 64), dtype=torch.bfloat16, device="cuda"))
+    with pytest.raises(ValueError):
+        fa.fa_fwd(q, q, q, lse=torch.empty((1, 2, 100), device="cuda"))
+    mask = torch.ones((2, 2), dtype=torch.uint8, device="cuda")
+    with pytest.raises(ValueError):
+        fa.fa_fwd_sparse(q, q[:, :, :128].contiguous(), q, mask)
+    with pytest.raises(ValueError):
+        fa.fa_fwd_sparse(q, q, q, mask, o=torch.empty((1, 2, 200, 32), dtype=torch.bfloat16, device="cuda"))
+    dq = torch.zeros((2, 4, 64), dtype=torch.bfloat16, device="cuda")
+    cache = torch.zeros((2, 4, 300, 64), dtype=torch.bfloat16, device="cuda")
+    sl = torch.full((2,), 300, dtype=torch.int32, device="cuda")
+    with pytest.raises(ValueError):
+        fa.fa_decode(dq, cache, cache, sl, 2, o=torch.empty((2, 4, 32), dtype=torch.bfloat16, device="cuda"))
+    with pytest.raises(ValueError):
+        fa.fa_decode(dq, cache, cache, sl, 2, lse=torch.empty((2, 3), device="cuda"))
+    with pytest.raises(ValueError):
+        fa.fa_decode_gqa(dq, cache[:, :2].contiguous(), cache[:, :2].contiguous(), sl, 2,
+                         lse=torch.empty((2, 2), device="cuda"))
+    q8 = torch.zeros((1, 2, 200, 128), dtype=torch.uint8, device="cuda")
+    vt8 = torch.zeros((1, 2, 128, 208), dtype=torch.uint8, device="cuda")
+    good = torch.ones((1, 2, 2), device="cuda")
+    with pytest.raises(ValueError):
+        fa.fa_fwd_fp8(q8, q8, vt8, torch.ones((1, 2, 1), device="cuda"), good, torch.ones((1, 2), device="cuda"))
+    with pytest.raises(ValueError):
+        fa.fa_fwd_fp8(q8, q8, vt8, good, good, torch.ones((1, 2, 2), device="cuda"))
+    torch.cuda.synchronize()
+    fa.fa_check_device_error()
+
+
 def test_python_binding_rejects_bad_tensors():
     import exact_attention_29_gb300 as fa
 
