@@ -579,6 +579,10 @@ def run_gpu(args, world, rank, local):
         "clocks": clocks,
     }
     print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
 
 
 def main():

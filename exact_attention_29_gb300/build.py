@@ -13,6 +13,8 @@ FA_LIBRARY names it.
 from __future__ import annotations
 
 import concurrent.futures as cf
+import contextlib
+import fcntl
 import os
 import shutil
 import subprocess
@@ -45,14 +47,33 @@ def _newest_input() -> float:
     return max(os.path.getmtime(p) for p in paths)
 
 
+@contextlib.contextmanager
+def _exclusive(path: str):
+    """Serialise builds: several processes (one per rank) may call build() at once."""
+    with open(path, "w") as f:
+        fcntl.flock(f, fcntl.LOCK_EX)
+        try:
+            yield
+        finally:
+            fcntl.flock(f, fcntl.LOCK_UN)
+
+
 def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False, debug: bool = False) -> str:
     """Compile every translation unit and link libfa.so (libfa_debug.so with
     debug=True); returns its path."""
     lib_path, out_dir = (DEBUG_LIB, DEBUG_OUT_DIR) if debug else (LIB, OUT_DIR)
     if not force and os.path.exists(lib_path) and os.path.getmtime(lib_path) >= _newest_input():
         return lib_path
-    nvcc = _nvcc()
     os.makedirs(out_dir, exist_ok=True)
+    with _exclusive(os.path.join(out_dir, ".build.lock")):
+        # another process may have built it while this one waited
+        if not force and os.path.exists(lib_path) and os.path.getmtime(lib_path) >= _newest_input():
+            return lib_path
+        return _build_locked(lib_path, out_dir, verbose, ptxas_info, debug)
+
+
+def _build_locked(lib_path: str, out_dir: str, verbose: bool, ptxas_info: bool, debug: bool) -> str:
+    nvcc = _nvcc()
     extra = ["-Xptxas", "-v"] if ptxas_info else []
     if debug:
         extra = extra + ["-DFA_DEBUG"]
