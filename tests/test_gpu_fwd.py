@@ -38,6 +38,17 @@ def test_small_shapes_full_oracle(N, d, causal):
     compare(o, lse, o_ref, lse_ref, f"N={N} d={d} causal={causal}")
 
 
+@pytest.mark.parametrize("causal", [False, True])
+def test_item_count_just_over_the_grid(causal):
+    """B=7, H=11, N=700: 77 heads x 2 Q-tile pairs = 154 work items for 152
+    persistent CTAs, so two CTAs take a second item (dealt in reverse), and the
+    last pair of every head has a ragged second tile."""
+    q, k, v = wl.prefill_inputs(7, 11, 700, 64, seed=77)
+    o, lse = _run(q, k, v, causal)
+    o_ref, lse_ref = oracle.attention(q, k, v, causal, 64 ** -0.5)
+    compare(o, lse, o_ref, lse_ref, f"7x11x700 causal={causal}")
+
+
 def test_pr1_config():
     """B=1, H=1, N=128, d=64, non-causal, seed 0 — the smallest named workload."""
     c = wl.PREFILL["pr1"]
