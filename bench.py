@@ -408,58 +408,39 @@ def run_gpu(args, world, rank, local):
     gqa_gbs = world * gqa_kv * gqa_steps / (gqa_ms * 1e-3) / 1e9
     del gkc, gvc
 
-    # end to end through the public API with pinned host buffers. Every step
-    # uploads its q, k, v from pinned host memory, calls fa_fwd and downloads o
-    # and lse, all inside the timed region. Steps are double-buffered over three
-    # streams, as a serving pipeline would run them: step s+1's upload and step
-    # s-1's download overlap step s's kernel.
+    # end to end through the C ABI with host buffers: every step is one
+    # fa_fwd_host call, which uploads q, k, v from pinned host memory, runs the
+    # forward and downloads o and lse, all inside the timed region. Steps go
+    # round-robin over three streams, as a serving pipeline would issue them,
+    # so step s+1's upload and step s-1's download overlap step s's kernel.
     hq, hk, hv = (t.cpu().pin_memory() for t in (q, k, v))
-    bufs_in = [tuple(torch.empty_like(t) for t in (q, k, v)) for _ in range(2)]
-    bufs_out = [(torch.empty_like(o), torch.empty_like(lse)) for _ in range(2)]
+    e2e_streams = [torch.cuda.Stream(dev) for _ in range(3)]
     hosts_out = [(torch.empty(o.shape, dtype=o.dtype).pin_memory(), torch.empty(lse.shape, dtype=lse.dtype).pin_memory())
-                 for _ in range(2)]
-    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
-    ev_in = [torch.cuda.Event() for _ in range(2)]
-    ev_cmp = [torch.cuda.Event() for _ in range(2)]
-    ev_out = [torch.cuda.Event() for _ in range(2)]
-    e2e_steps = max(2, min(args.steps, 20))
+                 for _ in range(3)]
+    e2e_steps = max(3, min(args.steps, 20))
 
     def e2e_run(steps, e_start=None, e_end=None):
+        s0 = e2e_streams[0]
         if e_start is not None:
-            e_start.record(s_in)
+            e_start.record(s0)
+            for st in e2e_streams[1:]:
+                st.wait_stream(s0)
         for s in range(steps):
-            b = s % 2
-            qb, kb, vb = bufs_in[b]
-            ob, lb = bufs_out[b]
-            if s >= 2:
-                s_in.wait_event(ev_cmp[b])  # step s-2's kernel has read this input buffer
-            with torch.cuda.stream(s_in):
-                qb.copy_(hq, non_blocking=True)
-                kb.copy_(hk, non_blocking=True)
-                vb.copy_(hv, non_blocking=True)
-            ev_in[b].record(s_in)
-            stream.wait_event(ev_in[b])
-            if s >= 2:
-                stream.wait_event(ev_out[b])  # step s-2's download has read this output buffer
-            fa.fa_fwd(qb, kb, vb, causal=pc.causal, o=ob, lse=lb, stream=stream)
-            ev_cmp[b].record(stream)
-            s_out.wait_event(ev_cmp[b])
-            with torch.cuda.stream(s_out):
-                hosts_out[b][0].copy_(ob, non_blocking=True)
-                hosts_out[b][1].copy_(lb, non_blocking=True)
-            ev_out[b].record(s_out)
+            ho, hl = hosts_out[s % 3]
+            fa.fa_fwd_host(hq, hk, hv, causal=pc.causal, o=ho, lse=hl, stream=e2e_streams[s % 3])
         if e_end is not None:
-            s_out.wait_stream(s_in)
-            s_out.wait_stream(stream)
-            e_end.record(s_out)
+            for st in e2e_streams[1:]:
+                s0.wait_stream(st)
+            e_end.record(s0)
 
-    e2e_run(2)
+    e2e_run(3)
     torch.cuda.synchronize(dev)
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e2e_run(e2e_steps, e0, e1)
     torch.cuda.synchronize(dev)
-    fa.fa_check_device_error(stream)
+    for st in e2e_streams:
+        fa.fa_check_device_error(st)
     e2e_ms = reduce_max([e0.elapsed_time(e1)], world)[0]
     e2e_value = world * fwd_flops * e2e_steps / (e2e_ms * 1e-3) / 1e12
     h2d = sum(t.numel() * t.element_size() for t in (q, k, v))
@@ -467,13 +448,17 @@ def run_gpu(args, world, rank, local):
 
     # the host link alone: one step's uploads and downloads, at the same time on
     # the same two streams, no kernel; the pipeline above cannot beat this
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    d_in = tuple(torch.empty_like(t) for t in (q, k, v))
+    d_out = (torch.empty_like(o), torch.empty_like(lse))
+
     def link_step():
         with torch.cuda.stream(s_in):
-            for dst, src in zip(bufs_in[0], (hq, hk, hv)):
+            for dst, src in zip(d_in, (hq, hk, hv)):
                 dst.copy_(src, non_blocking=True)
         with torch.cuda.stream(s_out):
-            hosts_out[0][0].copy_(bufs_out[0][0], non_blocking=True)
-            hosts_out[0][1].copy_(bufs_out[0][1], non_blocking=True)
+            hosts_out[0][0].copy_(d_out[0], non_blocking=True)
+            hosts_out[0][1].copy_(d_out[1], non_blocking=True)
 
     link_step()
     torch.cuda.synchronize(dev)
@@ -487,7 +472,7 @@ def run_gpu(args, world, rank, local):
     l1.record(s_out)
     torch.cuda.synchronize(dev)
     link_ms = l0.elapsed_time(l1) / 5
-    del bufs_in, bufs_out
+    del d_in, d_out
 
     if rank != 0:
         return
@@ -572,9 +557,10 @@ def run_gpu(args, world, rank, local):
                          "frac": link_ms / (e2e_ms / e2e_steps),
                          "what": "one step's uploads and downloads alone (same streams, no kernel): the host "
                                  "link's bound on a step; frac = that time / the pipelined step time"},
-                "what": "prefill through fa_fwd with pinned host buffers; every step uploads q/k/v and downloads "
-                        "o/lse inside the timed region, double-buffered over three streams (upload of step s+1 "
-                        "and download of step s-1 overlap step s)"},
+                "what": "prefill through the C-ABI call fa_fwd_host with pinned host buffers; every step's call "
+                        "uploads q/k/v, runs the forward and downloads o/lse inside the timed region; steps go "
+                        "round-robin over three streams (upload of step s+1 and download of step s-1 overlap "
+                        "step s)"},
         "gpu_launches": 3 * args.steps,
         "clocks": clocks,
     }

@@ -22,6 +22,7 @@ from ._lib import (  # noqa: F401
     fa_decode_noalloc,
     fa_fwd,
     fa_fwd_fp8,
+    fa_fwd_host,
     fa_fwd_sparse,
     fa_fwd_sparse_plan,
     fa_quantize_fp8,

@@ -32,6 +32,7 @@ _VP = ctypes.c_void_p
 _I = ctypes.c_int
 _SIGNATURES = {
     "fa_fwd": ([_VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, ctypes.c_float, _VP], _I),
+    "fa_fwd_host": ([_VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, ctypes.c_float, _VP], _I),
     "fa_decode": ([_VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _VP], _I),
     "fa_bwd": ([_VP] * 9 + [_I] * 5 + [ctypes.c_float, _VP], _I),
     "fa_decode_gqa": ([_VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _I, _VP], _I),
@@ -135,6 +136,37 @@ def fa_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = Fal
     st = lib.fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), B, H, N, d,
                     1 if causal else 0, float(scale), _stream_handle(stream))
     _check(st, "fa_fwd")
+    return o, lse
+
+
+def fa_fwd_host(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = False, scale: float | None = None,
+                o: torch.Tensor | None = None, lse: torch.Tensor | None = None, stream=None):
+    """fa_fwd on HOST tensors: q, k, v bf16 [B, H, N, d] in CPU memory (pinned
+    for asynchronous copies). The library uploads them, runs the forward and
+    downloads o and lse, all enqueued on ``stream``; the results are valid once
+    the stream has passed the call. Returns (o, lse) as CPU tensors (pinned when
+    allocated here)."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        if not isinstance(t, torch.Tensor) or t.device.type != "cpu":
+            raise ValueError(f"{n} must be a CPU tensor")
+        if t.dtype != torch.bfloat16 or t.dim() != 4 or not t.is_contiguous():
+            raise ValueError(f"{n} must be a contiguous bf16 tensor [B, H, N, d]")
+    if k.shape != q.shape or v.shape != q.shape:
+        raise ValueError("q, k and v must have the same shape [B, H, N, d]")
+    B, H, N, d = q.shape
+    if scale is None:
+        scale = d ** -0.5
+    if o is None:
+        o = torch.empty(q.shape, dtype=torch.bfloat16).pin_memory()
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32).pin_memory()
+    for t, n, dt, shp in ((o, "o", torch.bfloat16, q.shape), (lse, "lse", torch.float32, (B, H, N))):
+        if t.device.type != "cpu" or t.dtype != dt or tuple(t.shape) != tuple(shp) or not t.is_contiguous():
+            raise ValueError(f"{n} must be a contiguous CPU {dt} tensor of shape {tuple(shp)}")
+    lib = load_library()
+    st = lib.fa_fwd_host(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), B, H, N, d,
+                         1 if causal else 0, float(scale), _stream_handle(stream))
+    _check(st, "fa_fwd_host")
     return o, lse
 
 

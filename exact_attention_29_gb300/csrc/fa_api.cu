@@ -96,6 +96,13 @@ fa_status ws_alloc(int dev, void** ptr, size_t bytes, cudaStream_t stream, const
         uint64_t keep = kPoolKeepBytes;
         e = cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &keep);
       }
+      if (e == cudaSuccess) {
+        // An allocation may not reuse a block still pending release on another
+        // stream by making its stream wait for that one: such a hidden wait
+        // would serialise callers that pipeline steps over several streams.
+        int no = 0;
+        e = cudaMemPoolSetAttribute(pool, cudaMemPoolReuseAllowInternalDependencies, &no);
+      }
       if (e != cudaSuccess) {
         set_error_text("cudaMemPoolCreate(workspace pool)", e);
         return FA_ERR_CUDA;
@@ -230,6 +237,64 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
   if (!err) return FA_ERR_CUDA;
   return launch_fwd(q, k, v, o, lse, B, H, N, d, causal, scale, reinterpret_cast<cudaStream_t>(stream), err,
                     g_num_sms[dev]);
+}
+
+fa_status fa_fwd_host(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
+                      int causal, float scale, fa_stream_t stream) {
+  if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned4(lse)) return FA_ERR_INVALID_ARG;
+  if (B < 1 || H < 1 || N < 1 || d < 1) return FA_ERR_INVALID_ARG;
+  if (!(scale > 0.f) || !std::isfinite(scale)) return FA_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  const long long bh = static_cast<long long>(B) * H;
+  const long long pairs = (static_cast<long long>(N) + 255) / 256;
+  if (bh > 0x7fffffffLL || pairs > 65535) return FA_ERR_INVALID_ARG;
+  int dev = -1;
+  fa_status st = current_device(&dev);
+  if (st != FA_OK) return st;
+  unsigned int* err = device_error_word();
+  if (!err) return FA_ERR_CUDA;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  // one pool buffer: q, k, v, o (bf16, 256-byte multiples apart) then lse
+  const size_t tensor = static_cast<size_t>(bh) * N * d * 2;
+  const size_t slot = (tensor + 255) / 256 * 256;
+  const size_t lse_bytes = static_cast<size_t>(bh) * N * sizeof(float);
+  void* ws = nullptr;
+  st = ws_alloc(dev, &ws, 4 * slot + lse_bytes, s, "workspace allocation (host-buffer prefill)");
+  if (st != FA_OK) return st;
+  uint8_t* base = static_cast<uint8_t*>(ws);
+  void* dq = base;
+  void* dk = base + slot;
+  void* dv = base + 2 * slot;
+  void* dout = base + 3 * slot;
+  float* dlse = reinterpret_cast<float*>(base + 4 * slot);
+  cudaError_t e = cudaSuccess;
+  const char* what = nullptr;
+  if ((e = cudaMemcpyAsync(dq, q, tensor, cudaMemcpyHostToDevice, s)) != cudaSuccess) what = "cudaMemcpyAsync(q)";
+  else if ((e = cudaMemcpyAsync(dk, k, tensor, cudaMemcpyHostToDevice, s)) != cudaSuccess) what = "cudaMemcpyAsync(k)";
+  else if ((e = cudaMemcpyAsync(dv, v, tensor, cudaMemcpyHostToDevice, s)) != cudaSuccess) what = "cudaMemcpyAsync(v)";
+  if (what) {
+    set_error_text(what, e);
+    cudaFreeAsync(ws, s);
+    return FA_ERR_CUDA;
+  }
+  st = launch_fwd(dq, dk, dv, dout, dlse, B, H, N, d, causal, scale, s, err, g_num_sms[dev]);
+  if (st == FA_OK) {
+    if ((e = cudaMemcpyAsync(o, dout, tensor, cudaMemcpyDeviceToHost, s)) != cudaSuccess) what = "cudaMemcpyAsync(o)";
+    else if ((e = cudaMemcpyAsync(lse, dlse, lse_bytes, cudaMemcpyDeviceToHost, s)) != cudaSuccess)
+      what = "cudaMemcpyAsync(lse)";
+    if (what) {
+      set_error_text(what, e);
+      st = FA_ERR_CUDA;
+    }
+  }
+  e = cudaFreeAsync(ws, s);
+  if (st == FA_OK && e != cudaSuccess) {
+    set_error_text("cudaFreeAsync(host-buffer prefill)", e);
+    st = FA_ERR_CUDA;
+  }
+  return st;
 }
 
 fa_status fa_fwd_sparse(const void* q, const void* k, const void* v, const uint8_t* mask, int mask_heads, void* o,

@@ -77,6 +77,26 @@ fa_status fa_fwd(const void *q, const void *k, const void *v, void *o, float *ls
                  int causal, float scale, fa_stream_t stream);
 
 /*
+ * Prefill from and to host memory: fa_fwd with the host<->device copies inside
+ * the call. q, k, v and o, lse are HOST pointers with the layouts of fa_fwd.
+ * On `stream` the call enqueues: device buffers for q, k, v, o and lse from
+ * the library's stream-ordered pool; one cudaMemcpyAsync per input
+ * (host to device); the forward; one cudaMemcpyAsync per output (device to
+ * host); the release of the buffers. It returns without waiting.
+ *
+ * Ownership: the host buffers must stay valid, and the inputs unchanged, until
+ * the stream has passed the call (cudaStreamSynchronize or an event). With
+ * page-locked (pinned) host memory the copies are asynchronous and the calls
+ * of successive steps on different streams overlap their copies with each
+ * other's kernels; with pageable memory the copies still complete correctly but
+ * synchronise with the host.
+ * Errors: as fa_fwd (16-byte alignment applies to the host pointers too), plus
+ *   FA_ERR_CUDA if a copy or the pool allocation fails.
+ */
+fa_status fa_fwd_host(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H, int N, int d,
+                      int causal, float scale, fa_stream_t stream);
+
+/*
  * Block-sparse prefill forward.
  *
  * Defines: "FlashAttention 完全拆解（一）", block-sparse extension: given a

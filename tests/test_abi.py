@@ -6,6 +6,7 @@ import os
 import re
 
 import pytest
+import torch
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 HEADER = os.path.join(ROOT, "include", "fa.h")
@@ -67,6 +68,37 @@ def test_fwd_rejects_bad_arguments(lib):
     assert _fwd(lib, d=96) == fa.FA_ERR_UNSUPPORTED
     assert _fwd(lib, d=256) == fa.FA_ERR_UNSUPPORTED
     assert _fwd(lib, N=65536 * 256 + 1) == fa.FA_ERR_INVALID_ARG  # more Q-tile pairs than the grid allows
+
+
+def test_host_buffer_fwd_rejects_bad_arguments(lib):
+    """Argument checks run before any CUDA call, so they need no GPU."""
+    import exact_attention_29_gb300 as fa
+
+    def fwd_host(q=16, k=16, v=16, o=16, lse=16, B=1, H=1, N=128, d=64, causal=0, scale=0.125):
+        return lib.fa_fwd_host(q, k, v, o, lse, B, H, N, d, causal, scale, None)
+
+    assert fwd_host(v=None) == fa.FA_ERR_INVALID_ARG
+    assert fwd_host(o=None) == fa.FA_ERR_INVALID_ARG
+    assert fwd_host(q=8) == fa.FA_ERR_INVALID_ARG  # host pointers are held to 16 bytes too
+    assert fwd_host(lse=2) == fa.FA_ERR_INVALID_ARG
+    assert fwd_host(H=0) == fa.FA_ERR_INVALID_ARG
+    assert fwd_host(scale=-1.0) == fa.FA_ERR_INVALID_ARG
+    assert fwd_host(causal=-1) == fa.FA_ERR_INVALID_ARG
+    assert fwd_host(d=32) == fa.FA_ERR_UNSUPPORTED
+
+
+def test_host_buffer_binding_rejects_device_or_strided_tensors():
+    import exact_attention_29_gb300 as fa
+
+    q = torch.zeros(1, 1, 8, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        fa.fa_fwd_host(q.float(), q, q)
+    with pytest.raises(ValueError):
+        fa.fa_fwd_host(q, q.transpose(2, 3).contiguous(), q)
+    with pytest.raises(ValueError):
+        fa.fa_fwd_host(q.transpose(2, 3), q, q)
+    with pytest.raises(ValueError):
+        fa.fa_fwd_host(q, q, q, o=torch.zeros(1, 1, 8, 64), lse=torch.zeros(1, 1, 8))
 
 
 def test_decode_rejects_bad_arguments(lib):

@@ -186,6 +186,34 @@ def test_output_16_byte_aligned_only(d):
     compare(o_b, lse, o_ref, lse_ref, "16-byte aligned output")
 
 
+@pytest.mark.parametrize("pinned", [True, False])
+@pytest.mark.parametrize("causal", [False, True])
+def test_host_buffer_call_matches_device_call(pinned, causal):
+    """fa_fwd_host (host inputs and outputs, copies inside the call) gives the
+    same bits as fa_fwd on device copies of the same inputs, from pinned and
+    from pageable host memory, and matches the oracle."""
+    import exact_attention_29_gb300 as fa
+
+    q, k, v = wl.prefill_inputs(2, 3, 517, 128, seed=21 + int(causal))
+    if pinned:
+        q, k, v = q.pin_memory(), k.pin_memory(), v.pin_memory()
+        o_h = lse_h = None
+    else:
+        o_h = torch.full(q.shape, float("nan"), dtype=torch.bfloat16)
+        lse_h = torch.full((2, 3, 517), float("nan"))
+    s = torch.cuda.Stream()
+    o_h, lse_h = fa.fa_fwd_host(q, k, v, causal=causal, o=o_h, lse=lse_h, stream=s)
+    s.synchronize()
+    fa.fa_check_device_error(s)
+    assert o_h.device.type == "cpu" and o_h.is_pinned() == pinned
+    o_d, lse_d = _run(q, k, v, causal)
+    torch.cuda.synchronize()
+    assert torch.equal(o_h, o_d.cpu())
+    assert torch.equal(lse_h, lse_d.cpu())
+    o_ref, lse_ref = oracle.attention(q, k, v, causal, 128 ** -0.5)
+    compare(o_h, lse_h, o_ref, lse_ref, f"host buffers pinned={pinned} causal={causal}")
+
+
 def test_bindings_reject_wrong_shapes_before_any_launch():
     """The library takes raw pointers; the binding refuses tensors whose extent
     or device does not match (caller-provided outputs and scales included)."""
