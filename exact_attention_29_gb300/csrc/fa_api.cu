@@ -8,6 +8,7 @@
 #include <cstdint>
 #include <cstdio>
 #include <cstring>
+#include <initializer_list>
 #include <mutex>
 
 #include "fa_common.cuh"
@@ -239,6 +240,22 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
                     g_num_sms[dev]);
 }
 
+namespace {
+
+// True when the runtime knows `p` as memory of a device (not host, managed or
+// unregistered host memory). Such a pointer is refused where the call copies
+// from or to the host.
+bool device_memory(const void* p) {
+  cudaPointerAttributes a = {};
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return false;
+  }
+  return a.type == cudaMemoryTypeDevice;
+}
+
+}  // namespace
+
 fa_status fa_fwd_host(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
                       int causal, float scale, fa_stream_t stream) {
   if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
@@ -261,6 +278,12 @@ fa_status fa_fwd_host(const void* q, const void* k, const void* v, void* o, floa
   const size_t slot = (tensor + 255) / 256 * 256;
   const size_t lse_bytes = static_cast<size_t>(bh) * N * sizeof(float);
   void* ws = nullptr;
+  for (const void* p : {q, k, v, static_cast<const void*>(o), static_cast<const void*>(lse)}) {
+    if (device_memory(p)) {
+      set_error_text("fa_fwd_host: a buffer is device memory (use fa_fwd)", cudaErrorInvalidValue);
+      return FA_ERR_INVALID_ARG;
+    }
+  }
   st = ws_alloc(dev, &ws, 4 * slot + lse_bytes, s, "workspace allocation (host-buffer prefill)");
   if (st != FA_OK) return st;
   uint8_t* base = static_cast<uint8_t*>(ws);

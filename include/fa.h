@@ -90,8 +90,9 @@ fa_status fa_fwd(const void *q, const void *k, const void *v, void *o, float *ls
  * of successive steps on different streams overlap their copies with each
  * other's kernels; with pageable memory the copies still complete correctly but
  * synchronise with the host.
- * Errors: as fa_fwd (16-byte alignment applies to the host pointers too), plus
- *   FA_ERR_CUDA if a copy or the pool allocation fails.
+ * Errors: as fa_fwd (16-byte alignment applies to the host pointers too);
+ *   FA_ERR_INVALID_ARG also when the runtime knows one of the five pointers as
+ *   device memory; FA_ERR_CUDA if a copy or the pool allocation fails.
  */
 fa_status fa_fwd_host(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H, int N, int d,
                       int causal, float scale, fa_stream_t stream);

@@ -214,6 +214,26 @@ def test_host_buffer_call_matches_device_call(pinned, causal):
     compare(o_h, lse_h, o_ref, lse_ref, f"host buffers pinned={pinned} causal={causal}")
 
 
+def test_host_buffer_call_refuses_device_memory():
+    import exact_attention_29_gb300 as fa
+
+    lib = fa.load_library()
+    q = torch.zeros(1, 1, 128, 64, dtype=torch.bfloat16, device="cuda")
+    h = torch.zeros(1, 1, 128, 64, dtype=torch.bfloat16).pin_memory()
+    lse = torch.zeros(1, 1, 128).pin_memory()
+    st = lib.fa_fwd_host(h.data_ptr(), q.data_ptr(), h.data_ptr(), h.data_ptr(), lse.data_ptr(), 1, 1, 128, 64, 0,
+                         0.125, None)
+    assert st == fa.FA_ERR_INVALID_ARG
+    assert b"device memory" in lib.fa_last_error_string()
+    o = torch.full_like(h, float("nan")).pin_memory()
+    st = lib.fa_fwd_host(h.data_ptr(), h.data_ptr(), h.data_ptr(), o.data_ptr(), lse.data_ptr(), 1, 1, 128, 64, 0,
+                         0.125, None)
+    assert st == fa.FA_OK
+    torch.cuda.synchronize()
+    fa.fa_check_device_error()
+    assert torch.equal(o, h)  # zero V gives zero O
+
+
 def test_bindings_reject_wrong_shapes_before_any_launch():
     """The library takes raw pointers; the binding refuses tensors whose extent
     or device does not match (caller-provided outputs and scales included)."""
