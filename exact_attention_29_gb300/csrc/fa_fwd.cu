@@ -251,15 +251,24 @@ __device__ void load_role(const CUtensorMap* tm_q, const CUtensorMap* tm_k, cons
           if (!ok) break;
         }
         uint8_t* dst = sm.ring + slot * C::kTileBytes;
-        mbar_arrive_expect_tx(&sm.kv_full[slot], C::kTileBytes);
+        // K_j (j >= 1) lands on the barrier of V_(j-1), whose expected bytes
+        // counted it, so the MMA thread waits once per step for V_(j-1) and
+        // K_j; its own barrier completes its phase with a plain arrival.
+        uint64_t* bar = &sm.kv_full[slot];
+        if (kind == 0 && j > 0) {
+          mbar_arrive(bar);
+          bar = &sm.kv_full[(ring - 1) % C::kStages];
+        } else {
+          mbar_arrive_expect_tx(bar, (kind == 1 && j + 1 < n_max) ? 2 * C::kTileBytes : C::kTileBytes);
+        }
         const CUtensorMap* map = kind ? tm_v : tm_k;
         if (F8 && kind) {
           // V^T: rows are d, the 128 keys of tile jt are the inner coordinate
-          tma_load_3d(dst, map, &sm.kv_full[slot], jt * kBN, 0, it.bh);
+          tma_load_3d(dst, map, bar, jt * kBN, 0, it.bh);
         } else {
 #pragma unroll
           for (int c = 0; c < C::kChunks; ++c)
-            tma_load_3d(dst + c * kChunkBytes, map, &sm.kv_full[slot], c * 64, jt * kBN, it.bh);
+            tma_load_3d(dst + c * kChunkBytes, map, bar, c * 64, jt * kBN, it.bh);
         }
         ++ring;
       }
@@ -336,9 +345,8 @@ __device__ void mma_role(const Smem& sm, uint32_t tmem, const FwdParams& p) {
     for (int j = 0; j < n_max && ok; ++j) {
       const uint32_t iv = base + 2 * j + 1;  // V_j
       const uint32_t ik = base + 2 * j + 2;  // K_{j+1}
-      ok = wait_kv(iv);
+      ok = wait_kv(iv);  // V_j, and K_{j+1} if the item has it (both land on V_j's barrier)
       if (!ok) break;
-      bool k_next = false;
       for (int t = 0; t < 2; ++t) {
         const int nt = it.n(t);
         if (j >= nt) continue;
@@ -354,12 +362,6 @@ __device__ void mma_role(const Smem& sm, uint32_t tmem, const FwdParams& p) {
         tc_fence_after();
         pv_product<D, F8>(tmem + C::o_col(t), tmem + C::s_col(t), slot_addr(iv), j > 0);
         if (j + 1 < nt) {
-          if (!k_next) {
-            ok = wait_kv(ik);
-            if (!ok) break;
-            tc_fence_after();
-            k_next = true;
-          }
           // issued after P V of the same tile: the tensor pipe runs them in order,
           // so P is read before the new S overwrites those columns
           qk_product<D, F8>(tmem + C::s_col(t), t ? qa1 : qa0, slot_addr(ik));
