@@ -467,8 +467,7 @@ __device__ void softmax_role(const Smem& sm, uint32_t tmem, const FwdParams& p, 
         // and the P values packed in place and stored over the first columns of
         // the S tile. O is rescaled afterwards, when the registers are free.
         uint32_t r[128];
-        tmem_ld_x64(s_tm, *reinterpret_cast<uint32_t(*)[64]>(&r[0]));
-        tmem_ld_x64(s_tm + 64, *reinterpret_cast<uint32_t(*)[64]>(&r[64]));
+        tmem_ld_x64x2(s_tm, s_tm + 64, r);
         if (lim < kBN) {
   #pragma unroll
           for (int c = 0; c < 128; ++c)
@@ -528,21 +527,21 @@ __device__ void softmax_role(const Smem& sm, uint32_t tmem, const FwdParams& p, 
           }
         }
       } else {
-        // bf16 inputs, pass 1: row maximum of the raw scores, 64 columns at a time
-        // (scale > 0, so the maximum commutes with the scaling). Holding all 128
-        // scores at once, as the e4m3 path does, makes this instance spill.
+        // bf16 inputs, pass 1: row maximum of the raw scores (scale > 0, so the
+        // maximum commutes with the scaling), both halves of the row loaded
+        // together. The exponentials reload the scores 64 at a time: holding all
+        // 128 through that pass, as the e4m3 path does, makes this instance spill.
         float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-  #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          uint32_t r[64];
-          tmem_ld_x64(s_tm + 64 * h, r);
+        {
+          uint32_t r[128];
+          tmem_ld_x64x2(s_tm, s_tm + 64, r);
           if (lim < kBN) {
   #pragma unroll
-            for (int c = 0; c < 64; ++c)
-              if (64 * h + c >= lim) r[c] = 0xff800000u;  // -inf
+            for (int c = 0; c < 128; ++c)
+              if (c >= lim) r[c] = 0xff800000u;  // -inf
           }
   #pragma unroll
-          for (int c = 0; c < 64; c += 8) {
+          for (int c = 0; c < 128; c += 8) {
   #pragma unroll
             for (int i = 0; i < 4; ++i)
               mx[i] = fmax3(mx[i], __uint_as_float(r[c + 2 * i]), __uint_as_float(r[c + 2 * i + 1]));
