@@ -79,7 +79,7 @@ fa_status current_device(int* dev_out) {
 // keeps up to kPoolKeepBytes mapped between calls (the default pool returns
 // its memory at every synchronisation, and mapping it again costs about
 // 0.1 ms per call). Allocation and release are stream-ordered.
-constexpr uint64_t kPoolKeepBytes = 1ull << 30;
+constexpr uint64_t kPoolKeepBytes = 4ull << 30;
 cudaMemPool_t g_pool[kMaxDevices] = {};
 
 fa_status ws_alloc(int dev, void** ptr, size_t bytes, cudaStream_t stream, const char* what) {
@@ -98,11 +98,16 @@ fa_status ws_alloc(int dev, void** ptr, size_t bytes, cudaStream_t stream, const
         e = cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &keep);
       }
       if (e == cudaSuccess) {
-        // An allocation may not reuse a block still pending release on another
-        // stream by making its stream wait for that one: such a hidden wait
-        // would serialise callers that pipeline steps over several streams.
+        // Blocks are reused by the stream that released them (and across an
+        // event dependency the caller made), never by making one stream wait for
+        // another nor by taking another stream's block as soon as it is free.
+        // A caller that pipelines steps over several streams then keeps one
+        // workspace per stream, instead of streams stealing blocks from each
+        // other, the pool growing in the middle of the pipeline, or hidden waits
+        // serialising the streams.
         int no = 0;
         e = cudaMemPoolSetAttribute(pool, cudaMemPoolReuseAllowInternalDependencies, &no);
+        if (e == cudaSuccess) e = cudaMemPoolSetAttribute(pool, cudaMemPoolReuseAllowOpportunistic, &no);
       }
       if (e != cudaSuccess) {
         set_error_text("cudaMemPoolCreate(workspace pool)", e);

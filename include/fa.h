@@ -15,7 +15,11 @@
  * Workspaces: calls that need scratch memory take it, ordered on `stream`,
  * from a memory pool the library creates on each device (cudaMemPoolCreate)
  * and give it back on the same stream before returning; the pool keeps up to
- * 1 GiB mapped between calls, so repeated calls do not map memory again.
+ * 4 GiB mapped between calls, so repeated calls do not map memory again. A
+ * block is reused by the stream that released it (or across an event
+ * dependency the caller made), never by making one stream wait for another:
+ * a caller that pipelines calls over several streams keeps one workspace per
+ * stream.
  *
  * Conventions for every call:
  *   - Tensor arguments are DEVICE pointers (memory of the current CUDA device),
