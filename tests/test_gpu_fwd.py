@@ -214,6 +214,33 @@ def test_host_buffer_call_matches_device_call(pinned, causal):
     compare(o_h, lse_h, o_ref, lse_ref, f"host buffers pinned={pinned} causal={causal}")
 
 
+def test_host_buffer_calls_pipelined_over_streams():
+    """Six fa_fwd_host calls issued round-robin over three streams without waiting
+    in between (each stream reuses its own workspace while the others' copies and
+    kernels are in flight): every call's outputs equal fa_fwd's on the same inputs."""
+    import exact_attention_29_gb300 as fa
+
+    streams = [torch.cuda.Stream() for _ in range(3)]
+    cases = []
+    for c in range(6):
+        q, k, v = (t.pin_memory() for t in wl.prefill_inputs(1, 4, 640, 128, seed=40 + c))
+        cases.append((q, k, v))
+    outs = []
+    for c, (q, k, v) in enumerate(cases):
+        o = torch.empty(q.shape, dtype=torch.bfloat16).pin_memory()
+        lse = torch.empty((1, 4, 640)).pin_memory()
+        fa.fa_fwd_host(q, k, v, causal=bool(c & 1), o=o, lse=lse, stream=streams[c % 3])
+        outs.append((o, lse))
+    torch.cuda.synchronize()
+    for st in streams:
+        fa.fa_check_device_error(st)
+    for c, ((q, k, v), (o, lse)) in enumerate(zip(cases, outs)):
+        o_d, lse_d = _run(q, k, v, bool(c & 1))
+        torch.cuda.synchronize()
+        assert torch.equal(o, o_d.cpu()), c
+        assert torch.equal(lse, lse_d.cpu()), c
+
+
 def test_host_buffer_call_refuses_device_memory():
     import exact_attention_29_gb300 as fa
 
