@@ -108,6 +108,7 @@ class ClockSampler:
             self.t1 = time.time()
 
     def stop(self):
+        """Stop sampling; returns the summary of the window between mark("start") and mark("end")."""
         if self.proc is None:
             return None
         time.sleep(0.15)
@@ -116,18 +117,26 @@ class ClockSampler:
             self.proc.wait(timeout=5)
         except subprocess.TimeoutExpired:
             self.proc.kill()
-        rows = []
+        self.rows = []
         for ts, line in self.lines:
             parts = [p.strip() for p in line.split(",")]
             if len(parts) < 8:
                 continue
-            rows.append((ts, parts))
-        inside = [r for ts, r in rows if self.t0 is not None and self.t0 - 0.06 <= ts <= (self.t1 or ts) + 0.06]
-        if not inside and rows:  # timed region shorter than the sampling period: nearest samples
-            mid = (self.t0 + self.t1) / 2 if self.t0 and self.t1 else rows[-1][0]
-            inside = [min(rows, key=lambda r: abs(r[0] - mid))[1]]
-        if not inside:
+            self.rows.append((ts, parts))
+        return self.summary(self.t0, self.t1)
+
+    def summary(self, t0, t1):
+        """Median SM clock, maximum clock and throttle reasons seen between host
+        times t0 and t1 (the nearest sample when the window is shorter than the
+        sampling period)."""
+        rows = getattr(self, "rows", None)
+        if not rows or t0 is None:
             return None
+        t1 = t1 or t0
+        inside = [r for ts, r in rows if t0 - 0.06 <= ts <= t1 + 0.06]
+        if not inside:
+            mid = (t0 + t1) / 2
+            inside = [min(rows, key=lambda r: abs(r[0] - mid))[1]]
 
         def num(x):
             try:
@@ -237,6 +246,148 @@ def run_reference(args, world, rank):
     print(json.dumps(line), flush=True)
 
 
+L2_BYTES = 129 * 2 ** 20  # GB300 L2 (126 MiB usable of 129 MB nominal; inputs above this stream from HBM)
+
+
+def time_leg(fn, iters, stream, flush=None):
+    """Device time of `iters` calls of fn() on `stream`, in ms per call, after 3
+    warm-up calls. With `flush` (a callable that writes a buffer larger than
+    L2), every call is timed alone between two events after a flush, so each
+    starts with its inputs out of L2; without it the calls run back to back
+    (inputs larger than L2)."""
+    import torch
+
+    for _ in range(3):
+        fn()
+    torch.cuda.synchronize()
+    if flush is None:
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(iters):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / iters
+    total = 0.0
+    pairs = []
+    for _ in range(iters):
+        flush()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        fn()
+        b.record(stream)
+        pairs.append((a, b))
+    torch.cuda.synchronize()
+    for a, b in pairs:
+        total += a.elapsed_time(b)
+    return total / iters
+
+
+# Per-configuration legs: (name, prefill workload or decode workload, splits, calls timed)
+PREFILL_LEGS = (("C1_pr1", "pr1", 200), ("C2a_gpt2_small", "gpt2_small", 100),
+                ("C2b_gpt2_small_causal", "gpt2_small_causal", 100),
+                ("C3_llama3_8b_prefill_noncausal", "llama3_8b_prefill_noncausal", 50),
+                ("C4_long_16k", "long_16k", 20), ("C4_long_64k", "long_64k", 4))
+DECODE_LEGS = tuple((f"C5_{name}_S{s}", name, s, 20) for name in ("decode_32k", "decode_32k_ragged")
+                    for s in (8, 16, 32))
+
+
+def run_config_legs(fa, wl, perfmodel, dev, stream, peaks, tag, dec_cache):
+    """Every synthetic configuration timed on its own: absolute time, throughput
+    and fraction of the measured and of the nominal peak; each leg keeps its host
+    time window, for the clocks sampled while it ran. Inputs smaller than L2 are
+    flushed out of it before each call."""
+    import torch
+
+    legs = {}
+    flush_buf = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+
+    def flush():
+        flush_buf.fill_(1.0)
+
+    for leg, name, iters in PREFILL_LEGS:
+        c = wl.PREFILL[name]
+        q, k, v = wl.prefill_inputs(c.B, c.H, c.N, c.d, seed=0, device=dev)
+        o = torch.empty_like(q)
+        lse = torch.empty((c.B, c.H, c.N), dtype=torch.float32, device=dev)
+        small = 4 * q.numel() * q.element_size() < L2_BYTES
+
+        def call():
+            fa.fa_fwd(q, k, v, causal=c.causal, o=o, lse=lse, stream=stream)
+
+        t0 = time.time()
+        ms = time_leg(call, iters, stream, flush if small else None)
+        t1 = time.time()
+        fa.fa_check_device_error(stream)
+        flops = perfmodel.fwd_flops(c.B, c.H, c.N, c.d, c.causal)
+        tf = flops / (ms * 1e-3) / 1e12
+        legs[leg] = {"ms": ms, "value": tf, "unit": "TFLOP/s", "frac": tf / peaks["bf16_tflops"],
+                     "frac_of_nominal": tf / NOMINAL_BF16_TFLOPS, "calls": iters,
+                     "l2": "flushed before each call" if small else "inputs larger than L2",
+                     "shape": f"B{c.B} H{c.H} N{c.N} d{c.d} {'causal' if c.causal else 'non-causal'}",
+                     "window": (t0, t1)}
+        del q, k, v, o, lse
+    dq, kc, vc = dec_cache
+    for leg, name, splits, iters in DECODE_LEGS:
+        c = wl.DECODE[name]
+        sl_host = wl.decode_seqlens(c.B, c.L, seed=0, ragged=c.ragged)
+        sl = sl_host.to(dev)
+        o = torch.empty_like(dq)
+        lse = torch.empty((c.B, c.H), dtype=torch.float32, device=dev)
+
+        def call():
+            fa.fa_decode(dq, kc, vc, sl, splits, o=o, lse=lse, stream=stream)
+
+        t0 = time.time()
+        ms = time_leg(call, iters, stream)
+        t1 = time.time()
+        fa.fa_check_device_error(stream)
+        kv = perfmodel.decode_kv_bytes(c.H, c.d, sl_host.tolist())
+        alg = perfmodel.decode_algorithmic_bytes(c.B, c.H, c.d, sl_host.tolist())
+        gbs = alg / (ms * 1e-3) / 1e9
+        legs[leg] = {"ms": ms, "value": gbs, "unit": "GB/s", "kv_gbs": kv / (ms * 1e-3) / 1e9,
+                     "frac": gbs / peaks["hbm_gbs"], "frac_of_nominal": gbs / NOMINAL_HBM_GBS, "calls": iters,
+                     "l2": "inputs larger than L2", "shape": f"B{c.B} H{c.H} L{c.L} d{c.d} splits {splits}"
+                     + (" ragged" if c.ragged else ""), "window": (t0, t1)}
+    del flush_buf
+    for leg in legs.values():
+        leg["peak_kind"] = ("burst bf16 " if leg["unit"] == "TFLOP/s" else "copy ") + tag
+    return legs
+
+
+def oracle_one_core():
+    """The oracle on one host core (OpenMP threads = 1): all of C1 and two heads
+    of each GPT-2-shaped configuration, every row; TFLOP/s under the GPU's FLOP
+    convention (causal halved), then the thread count restored."""
+    import oracle
+    from exact_attention_29_gb300 import perfmodel
+    from exact_attention_29_gb300 import workloads as wl
+
+    oracle.build()
+    before = oracle.set_threads(0)
+    out = {}
+    try:
+        oracle.set_threads(1)
+        for leg, name, heads in (("C1_pr1", "pr1", 1), ("C2a_gpt2_small", "gpt2_small", 2),
+                                 ("C2b_gpt2_small_causal", "gpt2_small_causal", 2)):
+            c = wl.PREFILL[name]
+            q, k, v = wl.prefill_inputs(c.B, c.H, c.N, c.d, seed=0)
+            qs = q.reshape(-1, c.N, c.d)[:heads].unsqueeze(0)
+            ks = k.reshape(-1, c.N, c.d)[:heads].unsqueeze(0)
+            vs = v.reshape(-1, c.N, c.d)[:heads].unsqueeze(0)
+            t0 = time.perf_counter()
+            oracle.attention(qs, ks, vs, c.causal, c.scale)
+            dt = time.perf_counter() - t0
+            flops = perfmodel.fwd_flops(1, heads, c.N, c.d, c.causal)
+            out[leg] = {"value": flops / dt / 1e12, "unit": "TFLOP/s", "seconds": dt,
+                        "sample": f"{heads} of {c.B * c.H} heads, all {c.N} rows"}
+    finally:
+        oracle.set_threads(before)
+    return out
+
+
 def run_gpu(args, world, rank, local):
     import torch
 
@@ -304,7 +455,6 @@ def run_gpu(args, world, rank, local):
     sampler.mark("end")
     if world > 1:
         dist.barrier()
-    clocks = sampler.stop() if rank == 0 else None
     fa.fa_check_device_error(stream)
 
     total_ms = t_start.elapsed_time(t_end)
@@ -331,11 +481,13 @@ def run_gpu(args, world, rank, local):
     torch.cuda.synchronize(dev)
     b0 = torch.cuda.Event(enable_timing=True)
     b1 = torch.cuda.Event(enable_timing=True)
+    w_bwd = [time.time()]
     b0.record(stream)
     for _ in range(bwd_steps):
         bwd_step()
     b1.record(stream)
     torch.cuda.synchronize(dev)
+    w_bwd.append(time.time())
     fa.fa_check_device_error(stream)
     bwd_ms = reduce_max([b0.elapsed_time(b1)], world)[0]
     bwd_flops = perfmodel.bwd_flops(pc.B, pc.H, pc.N, pc.d, pc.causal)
@@ -355,11 +507,13 @@ def run_gpu(args, world, rank, local):
     f0 = torch.cuda.Event(enable_timing=True)
     f1 = torch.cuda.Event(enable_timing=True)
     fp8_steps = max(1, min(args.steps, 100))
+    w_fp8 = [time.time()]
     f0.record(stream)
     for _ in range(fp8_steps):
         fa.fa_fwd_fp8(q8, k8, vt8, qsc, ksc, vsc, causal=pc.causal, o=o8, lse=l8, stream=stream)
     f1.record(stream)
     torch.cuda.synchronize(dev)
+    w_fp8.append(time.time())
     fa.fa_check_device_error(stream)
     fp8_ms = reduce_max([f0.elapsed_time(f1)], world)[0]
     fp8_value = world * fwd_flops * fp8_steps / (fp8_ms * 1e-3) / 1e12
@@ -376,11 +530,13 @@ def run_gpu(args, world, rank, local):
     s0 = torch.cuda.Event(enable_timing=True)
     s1 = torch.cuda.Event(enable_timing=True)
     sparse_steps = max(1, min(args.steps, 100))
+    w_sparse = [time.time()]
     s0.record(stream)
     for _ in range(sparse_steps):
         fa.fa_fwd_sparse(q, k, v, smask_d, causal=sc.causal, o=o8, lse=l8, stream=stream)
     s1.record(stream)
     torch.cuda.synchronize(dev)
+    w_sparse.append(time.time())
     fa.fa_check_device_error(stream)
     sparse_ms = reduce_max([s0.elapsed_time(s1)], world)[0]
     sparse_flops = 4.0 * 128 * 128 * sc.d * s_allowed
@@ -397,16 +553,23 @@ def run_gpu(args, world, rank, local):
     g0 = torch.cuda.Event(enable_timing=True)
     g1 = torch.cuda.Event(enable_timing=True)
     gqa_steps = max(1, min(args.steps, 50))
+    w_gqa = [time.time()]
     g0.record(stream)
     for _ in range(gqa_steps):
         fa.fa_decode_gqa(gq, gkc, gvc, gsl, GQA_SPLITS, o=go, lse=glse, stream=stream)
     g1.record(stream)
     torch.cuda.synchronize(dev)
+    w_gqa.append(time.time())
     fa.fa_check_device_error(stream)
     gqa_ms = reduce_max([g0.elapsed_time(g1)], world)[0]
     gqa_kv = perfmodel.decode_kv_bytes(gc.Hkv, gc.d, gsl.tolist())
     gqa_gbs = world * gqa_kv * gqa_steps / (gqa_ms * 1e-3) / 1e9
     del gkc, gvc
+
+    # every synthetic configuration on its own (C1-C5; C3 causal is the step's prefill above)
+    peaks = _peaks()
+    tag = "of measured" if peaks["source"] == "measured" else "of fallback"
+    legs = run_config_legs(fa, wl, perfmodel, dev, stream, peaks, tag, (dq, kc, vc))
 
     # end to end through the C ABI with host buffers: every step is one
     # fa_fwd_host call, which uploads q, k, v from pinned host memory, runs the
@@ -476,10 +639,13 @@ def run_gpu(args, world, rank, local):
 
     if rank != 0:
         return
-    peaks = _peaks()
+    clocks = sampler.stop()
+    for leg in legs.values():
+        leg["clocks"] = sampler.summary(*leg.pop("window"))
+    leg_clocks = {name: sampler.summary(*w) for name, w in
+                  (("backward", w_bwd), ("fwd_fp8", w_fp8), ("fwd_sparse", w_sparse), ("decode_gqa", w_gqa))}
     long_region = total_ms > 1000.0
     tflops_peak = peaks["bf16_tflops_sustained"] if long_region else peaks["bf16_tflops"]
-    tag = "of measured" if peaks["source"] == "measured" else "of fallback"
     traffic = _profile_traffic()
     fwd_avg_ms = fwd_ms / args.steps
     dec_avg_ms = dec_ms / args.steps
@@ -519,6 +685,36 @@ def run_gpu(args, world, rank, local):
     }
 
     c_tflops, c_dt, _, c_desc = cpu_oracle_sample(args.cpu_heads)
+    one_core = oracle_one_core()
+    for name, lc in leg_clocks.items():
+        leg_roofs[name]["clocks"] = lc
+
+    def row(ms, val, unit, frac, frac_nom, clk):
+        return [float(f"{ms:.4g}"), float(f"{val:.4g}"), unit, round(frac, 3), round(frac_nom, 3),
+                (clk or {}).get("sm_mhz")]
+
+    summary = {"fields": "ms per call, value, unit (TF = TFLOP/s, GB = GB/s), frac of measured peak, "
+                         "frac of nominal (2.25 PF bf16, 7.9 TB/s), median SM MHz"}
+    for name in ("C1_pr1", "C2a_gpt2_small", "C2b_gpt2_small_causal"):
+        g = legs[name]
+        summary[name] = row(g["ms"], g["value"], "TF", g["frac"], g["frac_of_nominal"], g["clocks"])
+    summary["C3_llama3_8b_prefill"] = row(fwd_avg_ms, value / world, "TF", value / world / peaks["bf16_tflops"],
+                                          value / world / NOMINAL_BF16_TFLOPS, clocks)
+    for name, g in legs.items():
+        if name not in summary:
+            summary[name] = row(g["ms"], g["value"], "TF" if g["unit"] == "TFLOP/s" else "GB", g["frac"],
+                                g["frac_of_nominal"], g["clocks"])
+    summary["backward"] = row(bwd_ms / bwd_steps, bwd_value / world, "TF", leg_roofs["backward"]["frac"],
+                              bwd_value / world / NOMINAL_BF16_TFLOPS, leg_clocks["backward"])
+    summary["fwd_fp8"] = row(fp8_ms / fp8_steps, fp8_value / world, "TF", leg_roofs["fwd_fp8"]["frac"],
+                             fp8_value / world / (2 * NOMINAL_BF16_TFLOPS), leg_clocks["fwd_fp8"])
+    summary["fwd_sparse_kept"] = row(sparse_ms / sparse_steps, sparse_value / world, "TF",
+                                     leg_roofs["fwd_sparse"]["frac"], sparse_value / world / NOMINAL_BF16_TFLOPS,
+                                     leg_clocks["fwd_sparse"])
+    summary["fwd_sparse_computed_over_kept"] = round(s_computed / max(1, s_allowed), 3)
+    summary["decode_gqa"] = row(gqa_ms / gqa_steps, leg_roofs["decode_gqa"]["achieved"], "GB",
+                                leg_roofs["decode_gqa"]["frac"], leg_roofs["decode_gqa"]["achieved"] / NOMINAL_HBM_GBS,
+                                leg_clocks["decode_gqa"])
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": max(3, args.warmup), "ms_per_step": total_ms / args.steps, "higher_is_better": True,
@@ -550,7 +746,8 @@ def run_gpu(args, world, rank, local):
         "roofline": dominant,
         "rooflines": {"fwd": fwd_roof, "decode": dec_roof},
         "cpu_baseline": {"value": c_tflops, "unit": "TFLOP/s", "cores": _cores(), "kind": "oracle",
-                         "sample": c_desc, "seconds": c_dt},
+                         "sample": c_desc, "seconds": c_dt, "one_core": one_core},
+        "configs": legs,
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "steps": e2e_steps,
                 "link": {"ms_per_step": link_ms, "h2d_gbs": h2d / (link_ms * 1e-3) / 1e9,
@@ -562,6 +759,7 @@ def run_gpu(args, world, rank, local):
                         "round-robin over three streams (upload of step s+1 and download of step s-1 overlap "
                         "step s)"},
         "gpu_launches": 3 * args.steps,
+        "summary": summary,
         "clocks": clocks,
     }
     print(json.dumps(line), flush=True)

@@ -25,6 +25,7 @@ from ._lib import (  # noqa: F401
     fa_fwd_host,
     fa_fwd_sparse,
     fa_fwd_sparse_plan,
+    fa_last_error_site,
     fa_quantize_fp8,
     fa_fwd_plan,
     fa_selftest_mma,

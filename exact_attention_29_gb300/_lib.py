@@ -44,7 +44,8 @@ _SIGNATURES = {
     "fa_decode_noalloc": ([_VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _VP], _I),
     "fa_status_string": ([_I], ctypes.c_char_p),
     "fa_last_error_string": ([], ctypes.c_char_p),
-    "fa_check_device_error": ([_VP, ctypes.POINTER(_I)], _I),
+    "fa_check_device_error": ([_VP], _I),
+    "fa_last_error_site": ([], _I),
     "fa_fwd_plan": ([_I, _I, _I, ctypes.POINTER(ctypes.c_longlong), ctypes.POINTER(ctypes.c_longlong)], _I),
     "fa_selftest_mma": ([_I, _VP, _VP, _VP, _I, _I, _VP], _I),
     "fa_selftest_wait_timeout": ([ctypes.c_uint, _VP], _I),
@@ -56,7 +57,7 @@ class FaError(RuntimeError):
         self.status = status
         lib = _lib
         text = lib.fa_status_string(status).decode() if lib else str(status)
-        detail = lib.fa_last_error_string().decode() if (lib and status == FA_ERR_CUDA) else ""
+        detail = lib.fa_last_error_string().decode() if (lib and status != FA_OK) else ""
         super().__init__(f"{where}: {text}" + (f" [{detail}]" if detail else ""))
 
 
@@ -111,6 +112,22 @@ def _require_shape(t: torch.Tensor, name: str, dtype, shape, device) -> None:
         raise ValueError(f"{name} must be on {device}, got {t.device}")
 
 
+def _same_device(device, **tensors) -> None:
+    """Every tensor the library is handed must live on `device` (the call's device)."""
+    for name, t in tensors.items():
+        if t.device != device:
+            raise ValueError(f"{name} must be on {device}, got {t.device}")
+
+
+def _on(device, stream):
+    """The library launches on the CUDA device that is current when it is called:
+    make the tensors' device current for the call, and refuse a stream of
+    another device."""
+    if stream is not None and getattr(stream, "device", device) != device:
+        raise ValueError(f"stream is on {stream.device}, the tensors on {device}")
+    return torch.cuda.device(device)
+
+
 def fa_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = False, scale: float | None = None,
            o: torch.Tensor | None = None, lse: torch.Tensor | None = None, stream=None):
     """Fused prefill attention. q, k, v: bf16 [B, H, N, d] on the GPU.
@@ -133,8 +150,9 @@ def fa_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = Fal
     for t, n in ((k, "k"), (v, "v"), (o, "o")):
         _require_shape(t, n, torch.bfloat16, q.shape, q.device)
     _require_shape(lse, "lse", torch.float32, (B, H, N), q.device)
-    st = lib.fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), B, H, N, d,
-                    1 if causal else 0, float(scale), _stream_handle(stream))
+    with _on(q.device, stream):
+        st = lib.fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), B, H, N, d,
+                        1 if causal else 0, float(scale), _stream_handle(stream))
     _check(st, "fa_fwd")
     return o, lse
 
@@ -196,8 +214,9 @@ def fa_fwd_sparse(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, mask: torch
         lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
     _require_shape(o, "o", torch.bfloat16, q.shape, q.device)
     _require_shape(lse, "lse", torch.float32, (B, H, N), q.device)
-    st = lib.fa_fwd_sparse(q.data_ptr(), k.data_ptr(), v.data_ptr(), mask.data_ptr(), mask.shape[0], o.data_ptr(),
-                           lse.data_ptr(), B, H, N, d, 1 if causal else 0, float(scale), _stream_handle(stream))
+    with _on(q.device, stream):
+        st = lib.fa_fwd_sparse(q.data_ptr(), k.data_ptr(), v.data_ptr(), mask.data_ptr(), mask.shape[0], o.data_ptr(),
+                               lse.data_ptr(), B, H, N, d, 1 if causal else 0, float(scale), _stream_handle(stream))
     _check(st, "fa_fwd_sparse")
     return o, lse
 
@@ -242,9 +261,11 @@ def fa_quantize_fp8(x: torch.Tensor, signs: torch.Tensor | None = None, per_head
     sp = 0
     if signs is not None:
         _require(signs, "signs", torch.float32, 1)
+        _same_device(x.device, signs=signs)
         sp = signs.data_ptr()
-    st = lib.fa_quantize_fp8(x.data_ptr(), sp, codes.data_ptr(), scales.data_ptr(), B, H, N, d, int(per_head),
-                             int(transpose), pitch if transpose else 0, _stream_handle(stream))
+    with _on(x.device, stream):
+        st = lib.fa_quantize_fp8(x.data_ptr(), sp, codes.data_ptr(), scales.data_ptr(), B, H, N, d, int(per_head),
+                                 int(transpose), pitch if transpose else 0, _stream_handle(stream))
     _check(st, "fa_quantize_fp8")
     return codes, scales
 
@@ -274,9 +295,10 @@ def fa_fwd_fp8(q8: torch.Tensor, k8: torch.Tensor, vt8: torch.Tensor, q_scale: t
         lse = torch.empty((B, H, N), dtype=torch.float32, device=q8.device)
     _require_shape(o, "o", torch.bfloat16, (B, H, N, d), q8.device)
     _require_shape(lse, "lse", torch.float32, (B, H, N), q8.device)
-    st = lib.fa_fwd_fp8(q8.data_ptr(), k8.data_ptr(), vt8.data_ptr(), q_scale.data_ptr(), k_scale.data_ptr(),
-                        v_scale.data_ptr(), o.data_ptr(), lse.data_ptr(), B, H, N, d, 1 if causal else 0,
-                        float(scale), vt8.shape[3], _stream_handle(stream))
+    with _on(q8.device, stream):
+        st = lib.fa_fwd_fp8(q8.data_ptr(), k8.data_ptr(), vt8.data_ptr(), q_scale.data_ptr(), k_scale.data_ptr(),
+                            v_scale.data_ptr(), o.data_ptr(), lse.data_ptr(), B, H, N, d, 1 if causal else 0,
+                            float(scale), vt8.shape[3], _stream_handle(stream))
     _check(st, "fa_fwd_fp8")
     return o, lse
 
@@ -297,6 +319,7 @@ def fa_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor, l
     B, H, N, d = q.shape
     if lse.shape != (B, H, N):
         raise ValueError("lse must be [B, H, N]")
+    _same_device(q.device, k=k, v=v, o=o, lse=lse, dout=dout)
     if scale is None:
         scale = d ** -0.5
     dq = torch.empty_like(q) if dq is None else dq
@@ -306,9 +329,11 @@ def fa_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor, l
         _require(t, n, torch.bfloat16, 4)
         if t.shape != q.shape:
             raise ValueError(f"{n} must match q")
-    st = lib.fa_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), dout.data_ptr(),
-                    dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, N, d, 1 if causal else 0, float(scale),
-                    _stream_handle(stream))
+    _same_device(q.device, dq=dq, dk=dk, dv=dv)
+    with _on(q.device, stream):
+        st = lib.fa_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), dout.data_ptr(),
+                        dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, N, d, 1 if causal else 0, float(scale),
+                        _stream_handle(stream))
     _check(st, "fa_bwd")
     return dq, dk, dv
 
@@ -335,14 +360,16 @@ def fa_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, seq
     B, H, L, d = k_cache.shape
     if v_cache.shape != k_cache.shape or q.shape != (B, H, d) or seqlens.shape != (B,):
         raise ValueError("shapes must be q [B,H,d], caches [B,H,L,d], seqlens [B]")
+    _same_device(q.device, k_cache=k_cache, v_cache=v_cache, seqlens=seqlens)
     if o is None:
         o = torch.empty_like(q)
     if lse is None:
         lse = torch.empty((B, H), dtype=torch.float32, device=q.device)
     _require_shape(o, "o", torch.bfloat16, (B, H, d), q.device)
     _require_shape(lse, "lse", torch.float32, (B, H), q.device)
-    st = lib.fa_decode(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), seqlens.data_ptr(), o.data_ptr(),
-                       lse.data_ptr(), B, H, L, d, int(num_splits), _stream_handle(stream))
+    with _on(q.device, stream):
+        st = lib.fa_decode(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), seqlens.data_ptr(), o.data_ptr(),
+                           lse.data_ptr(), B, H, L, d, int(num_splits), _stream_handle(stream))
     _check(st, "fa_decode")
     return o, lse
 
@@ -366,14 +393,16 @@ def fa_decode_gqa(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
         raise ValueError("shapes must be q [B,Hq,d], caches [B,Hkv,L,d], seqlens [B]")
     if Hq % Hkv != 0:
         raise ValueError("Hq must be a multiple of Hkv")
+    _same_device(q.device, k_cache=k_cache, v_cache=v_cache, seqlens=seqlens)
     if o is None:
         o = torch.empty_like(q)
     if lse is None:
         lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
     _require_shape(o, "o", torch.bfloat16, (B, Hq, d), q.device)
     _require_shape(lse, "lse", torch.float32, (B, Hq), q.device)
-    st = lib.fa_decode_gqa(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), seqlens.data_ptr(), o.data_ptr(),
-                           lse.data_ptr(), B, Hq, Hkv, L, d, int(num_splits), _stream_handle(stream))
+    with _on(q.device, stream):
+        st = lib.fa_decode_gqa(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), seqlens.data_ptr(), o.data_ptr(),
+                               lse.data_ptr(), B, Hq, Hkv, L, d, int(num_splits), _stream_handle(stream))
     _check(st, "fa_decode_gqa")
     return o, lse
 
@@ -401,16 +430,16 @@ def fa_decode_noalloc(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Ten
     B, H, L, d = k_cache.shape
     if v_cache.shape != k_cache.shape or q.shape != (B, H, d) or seqlens.shape != (B,):
         raise ValueError("shapes must be q [B,H,d], caches [B,H,L,d], seqlens [B]")
+    _same_device(q.device, k_cache=k_cache, v_cache=v_cache, seqlens=seqlens)
     if o is None:
         o = torch.empty_like(q)
     if lse is None:
         lse = torch.empty((B, H), dtype=torch.float32, device=q.device)
     _require_shape(o, "o", torch.bfloat16, (B, H, d), q.device)
     _require_shape(lse, "lse", torch.float32, (B, H), q.device)
-    st = lib.fa_decode_noalloc(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), seqlens.data_ptr(),
-                               o.data_ptr(), lse.data_ptr(), B, H, L, d, int(num_splits), _stream_handle(stream))
-    if st == FA_ERR_INVALID_ARG:
-        raise FaError(st, "fa_decode_noalloc: " + lib.fa_last_error_string().decode())
+    with _on(q.device, stream):
+        st = lib.fa_decode_noalloc(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), seqlens.data_ptr(),
+                                   o.data_ptr(), lse.data_ptr(), B, H, L, d, int(num_splits), _stream_handle(stream))
     _check(st, "fa_decode_noalloc")
     return o, lse
 
@@ -419,14 +448,20 @@ def fa_check_device_error(stream=None) -> int:
     """Synchronise the stream and return the site code of a kernel wait that ran out
     (0 if none); raises FaError(FA_ERR_TIMEOUT) when one did."""
     lib = load_library()
-    site = ctypes.c_int(0)
-    st = lib.fa_check_device_error(_stream_handle(stream), ctypes.byref(site))
+    with torch.cuda.device(stream.device if stream is not None else torch.cuda.current_device()):
+        st = lib.fa_check_device_error(_stream_handle(stream))
+    site = lib.fa_last_error_site()
     if st in (FA_ERR_TIMEOUT, FA_ERR_CHECK):
-        err = FaError(st, f"fa_check_device_error (site {site.value})")
-        err.site = site.value
+        err = FaError(st, f"fa_check_device_error (site {site})")
+        err.site = site
         raise err
     _check(st, "fa_check_device_error")
-    return site.value
+    return site
+
+
+def fa_last_error_site() -> int:
+    """Site code read by the calling thread's most recent fa_check_device_error (0 if none)."""
+    return load_library().fa_last_error_site()
 
 
 def fa_fwd_plan(N: int, block: int = 128, causal: bool = False):
@@ -440,6 +475,7 @@ def fa_fwd_plan(N: int, block: int = 128, causal: bool = False):
 def fa_selftest_mma(mode: int, a: torch.Tensor, b: torch.Tensor, n: int, k: int, stream=None) -> torch.Tensor:
     lib = load_library()
     d = torch.empty((128, n), dtype=torch.float32, device=a.device)
+    _same_device(a.device, b=b)
     _check(lib.fa_selftest_mma(mode, a.data_ptr(), b.data_ptr(), d.data_ptr(), n, k, _stream_handle(stream)),
            "fa_selftest_mma")
     return d

@@ -23,6 +23,7 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 thread_local char t_error_text[512] = "";
+thread_local int t_error_site = 0;  // site of the last failed wait or check seen by fa_check_device_error
 
 std::mutex g_mutex;
 unsigned int* g_err_ptr[kMaxDevices] = {};
@@ -137,7 +138,15 @@ void set_error_text(const char* what, const char* detail) {
 
 unsigned int* device_error_word() {
   int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  const cudaError_t ge = cudaGetDevice(&dev);
+  if (ge != cudaSuccess) {
+    set_error_text("cudaGetDevice", ge);
+    return nullptr;
+  }
+  if (dev < 0 || dev >= kMaxDevices) {
+    set_error_text("device index", "out of range");
+    return nullptr;
+  }
   std::lock_guard<std::mutex> lock(g_mutex);
   if (g_err_ptr[dev] == nullptr) {
     void* p = nullptr;
@@ -205,6 +214,27 @@ bool encode_f32_map(CUtensorMap* map, const void* base, uint64_t d, uint64_t row
   return encode_3d(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 32, base, d, rows, outer, box_rows, d * 4);
 }
 
+fa_status reject(fa_status status, const char* failed_check) {
+  set_error_text("argument rejected", failed_check);
+  return status;
+}
+
+fa_status checked_device(int* dev) { return current_device(dev); }
+
+// The checks fa_decode and fa_decode_noalloc share.
+fa_status check_decode_args(const void* q, const void* k_cache, const void* v_cache, const int32_t* seqlens,
+                            const void* o, const float* lse, int B, int H, int L, int d, int num_splits) {
+  FA_REJECT_IF(!q || !k_cache || !v_cache || !seqlens || !o || !lse, FA_ERR_INVALID_ARG);
+  FA_REJECT_IF(!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned4(seqlens) || !aligned4(o) ||
+                   !aligned4(lse),
+               FA_ERR_INVALID_ARG);
+  FA_REJECT_IF(B < 1 || H < 1 || L < 1 || d < 1, FA_ERR_INVALID_ARG);
+  FA_REJECT_IF(num_splits < 1 || num_splits > 64, FA_ERR_INVALID_ARG);
+  FA_REJECT_IF(d != 64 && d != 128, FA_ERR_UNSUPPORTED);
+  FA_REJECT_IF(static_cast<long long>(B) * H > 0x7fffffffLL || H > 65535 || B > 65535, FA_ERR_INVALID_ARG);
+  return FA_OK;
+}
+
 }  // namespace fa
 
 using namespace fa;
@@ -225,17 +255,19 @@ const char* fa_status_string(fa_status status) {
 
 const char* fa_last_error_string(void) { return t_error_text; }
 
+int fa_last_error_site(void) { return t_error_site; }
+
 fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
                  int causal, float scale, fa_stream_t stream) {
-  if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
-  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned4(lse)) return FA_ERR_INVALID_ARG;
-  if (B < 1 || H < 1 || N < 1 || d < 1) return FA_ERR_INVALID_ARG;
-  if (!(scale > 0.f) || !std::isfinite(scale)) return FA_ERR_INVALID_ARG;
-  if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
-  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  FA_REJECT_IF(!q || !k || !v || !o || !lse, FA_ERR_INVALID_ARG);
+  FA_REJECT_IF(!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned4(lse), FA_ERR_INVALID_ARG);
+  FA_REJECT_IF(B < 1 || H < 1 || N < 1 || d < 1, FA_ERR_INVALID_ARG);
+  FA_REJECT_IF(!(scale > 0.f) || !std::isfinite(scale), FA_ERR_INVALID_ARG);
+  FA_REJECT_IF(causal != 0 && causal != 1, FA_ERR_INVALID_ARG);
+  FA_REJECT_IF(d != 64 && d != 128, FA_ERR_UNSUPPORTED);
   const long long bh = static_cast<long long>(B) * H;
   const long long pairs = (static_cast<long long>(N) + 255) / 256;
-  if (bh > 0x7fffffffLL || pairs > 65535) return FA_ERR_INVALID_ARG;
+  FA_REJECT_IF(bh > 0x7fffffffLL || pairs > 65535, FA_ERR_INVALID_ARG);
   int dev = -1;
   fa_status st = current_device(&dev);
   if (st != FA_OK) return st;
@@ -263,15 +295,15 @@ bool device_memory(const void* p) {
 
 fa_status fa_fwd_host(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
                       int causal, float scale, fa_stream_t stream) {
-  if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
-  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned4(lse)) return FA_ERR_INVALID_ARG;
-  if (B < 1 || H < 1 || N < 1 || d < 1) return FA_ERR_INVALID_ARG;
-  if (!(scale > 0.f) || !std::isfinite(scale)) return FA_ERR_INVALID_ARG;
-  if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
-  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  FA_REJECT_IF(!q || !k || !v || !o || !lse, FA_ERR_INVALID_ARG);
+  FA_REJECT_IF(!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned4(lse), FA_ERR_INVALID_ARG);
+  FA_REJECT_IF(B < 1 || H < 1 || N < 1 || d < 1, FA_ERR_INVALID_ARG);
+  FA_REJECT_IF(!(scale > 0.f) || !std::isfinite(scale), FA_ERR_INVALID_ARG);
+  FA_REJECT_IF(causal != 0 && causal != 1, FA_ERR_INVALID_ARG);
+  FA_REJECT_IF(d != 64 && d != 128, FA_ERR_UNSUPPORTED);
   const long long bh = static_cast<long long>(B) * H;
   const long long pairs = (static_cast<long long>(N) + 255) / 256;
-  if (bh > 0x7fffffffLL || pairs > 65535) return FA_ERR_INVALID_ARG;
+  FA_REJECT_IF(bh > 0x7fffffffLL || pairs > 65535, FA_ERR_INVALID_ARG);
   int dev = -1;
   fa_status st = current_device(&dev);
   if (st != FA_OK) return st;
@@ -327,16 +359,16 @@ fa_status fa_fwd_host(const void* q, const void* k, const void* v, void* o, floa
 
 fa_status fa_fwd_sparse(const void* q, const void* k, const void* v, const uint8_t* mask, int mask_heads, void* o,
                         float* lse, int B, int H, int N, int d, int causal, float scale, fa_stream_t stream) {
-  if (!q || !k || !v || !mask || !o || !lse) return FA_ERR_INVALID_ARG;
-  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned4(lse)) return FA_ERR_INVALID_ARG;
-  if (B < 1 || H < 1 || N < 1 || d < 1) return FA_ERR_INVALID_ARG;
-  if (mask_heads != 1 && mask_heads != H) return FA_ERR_INVALID_ARG;
-  if (!(scale > 0.f) || !std::isfinite(scale)) return FA_ERR_INVALID_ARG;
-  if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
-  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  FA_REJECT_IF(!q || !k || !v || !mask || !o || !lse, FA_ERR_INVALID_ARG);
+  FA_REJECT_IF(!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned4(lse), FA_ERR_INVALID_ARG);
+  FA_REJECT_IF(B < 1 || H < 1 || N < 1 || d < 1, FA_ERR_INVALID_ARG);
+  FA_REJECT_IF(mask_heads != 1 && mask_heads != H, FA_ERR_INVALID_ARG);
+  FA_REJECT_IF(!(scale > 0.f) || !std::isfinite(scale), FA_ERR_INVALID_ARG);
+  FA_REJECT_IF(causal != 0 && causal != 1, FA_ERR_INVALID_ARG);
+  FA_REJECT_IF(d != 64 && d != 128, FA_ERR_UNSUPPORTED);
   const long long bh = static_cast<long long>(B) * H;
   const long long pairs = (static_cast<long long>(N) + 255) / 256;
-  if (bh > 0x7fffffffLL || pairs > 65535) return FA_ERR_INVALID_ARG;
+  FA_REJECT_IF(bh > 0x7fffffffLL || pairs > 65535, FA_ERR_INVALID_ARG);
   int dev = -1;
   fa_status st = current_device(&dev);
   if (st != FA_OK) return st;
@@ -364,8 +396,8 @@ fa_status fa_fwd_sparse(const void* q, const void* k, const void* v, const uint8
 
 fa_status fa_fwd_sparse_plan(const uint8_t* mask, int mask_heads, int B, int H, int N, int causal,
                              long long* pairs_allowed, long long* pairs_computed) {
-  if (!mask || !pairs_allowed || !pairs_computed || B < 1 || H < 1 || N < 1) return FA_ERR_INVALID_ARG;
-  if (mask_heads != 1 && mask_heads != H) return FA_ERR_INVALID_ARG;
+  FA_REJECT_IF(!mask || !pairs_allowed || !pairs_computed || B < 1 || H < 1 || N < 1, FA_ERR_INVALID_ARG);
+  FA_REJECT_IF(mask_heads != 1 && mask_heads != H, FA_ERR_INVALID_ARG);
   const int T = (N + 127) / 128;
   long long allowed = 0, computed = 0;
   for (int h = 0; h < H; ++h) {
@@ -389,15 +421,16 @@ fa_status fa_fwd_sparse_plan(const uint8_t* mask, int mask_heads, int B, int H, 
 
 fa_status fa_quantize_fp8(const void* x, const float* signs, void* codes, float* scales, int B, int H, int N, int d,
                           int per_head, int transpose, int v_pitch, fa_stream_t stream) {
-  if (!x || !codes || !scales) return FA_ERR_INVALID_ARG;
-  if (!aligned16(x) || !aligned16(codes) || !aligned4(scales) || (signs && !aligned4(signs))) return FA_ERR_INVALID_ARG;
-  if (B < 1 || H < 1 || N < 1 || d < 1) return FA_ERR_INVALID_ARG;
-  if ((per_head != 0 && per_head != 1) || (transpose != 0 && transpose != 1)) return FA_ERR_INVALID_ARG;
-  if (transpose && (v_pitch < N || v_pitch % 16 != 0)) return FA_ERR_INVALID_ARG;
-  if (d != 128) return FA_ERR_UNSUPPORTED;
+  FA_REJECT_IF(!x || !codes || !scales, FA_ERR_INVALID_ARG);
+  FA_REJECT_IF(!aligned16(x) || !aligned16(codes) || !aligned4(scales) || (signs && !aligned4(signs)),
+               FA_ERR_INVALID_ARG);
+  FA_REJECT_IF(B < 1 || H < 1 || N < 1 || d < 1, FA_ERR_INVALID_ARG);
+  FA_REJECT_IF((per_head != 0 && per_head != 1) || (transpose != 0 && transpose != 1), FA_ERR_INVALID_ARG);
+  FA_REJECT_IF(transpose && (v_pitch < N || v_pitch % 16 != 0), FA_ERR_INVALID_ARG);
+  FA_REJECT_IF(d != 128, FA_ERR_UNSUPPORTED);
   const long long bh = static_cast<long long>(B) * H;
   const long long tiles = (static_cast<long long>(N) + 127) / 128;
-  if (bh > 65535 || tiles > 0x7fffffffLL) return FA_ERR_INVALID_ARG;
+  FA_REJECT_IF(bh > 65535 || tiles > 0x7fffffffLL, FA_ERR_INVALID_ARG);
   int dev = -1;
   fa_status st = current_device(&dev);
   if (st != FA_OK) return st;
@@ -420,18 +453,18 @@ fa_status fa_quantize_fp8(const void* x, const float* signs, void* codes, float*
 fa_status fa_fwd_fp8(const void* q8, const void* k8, const void* vt8, const float* q_scale, const float* k_scale,
                      const float* v_scale, void* o, float* lse, int B, int H, int N, int d, int causal, float scale,
                      int v_pitch, fa_stream_t stream) {
-  if (!q8 || !k8 || !vt8 || !q_scale || !k_scale || !v_scale || !o || !lse) return FA_ERR_INVALID_ARG;
-  if (!aligned16(q8) || !aligned16(k8) || !aligned16(vt8) || !aligned16(o) || !aligned4(lse) || !aligned4(q_scale) ||
-      !aligned4(k_scale) || !aligned4(v_scale))
-    return FA_ERR_INVALID_ARG;
-  if (B < 1 || H < 1 || N < 1 || d < 1) return FA_ERR_INVALID_ARG;
-  if (!(scale > 0.f) || !std::isfinite(scale)) return FA_ERR_INVALID_ARG;
-  if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
-  if (v_pitch < N || v_pitch % 16 != 0) return FA_ERR_INVALID_ARG;
-  if (d != 128) return FA_ERR_UNSUPPORTED;
+  FA_REJECT_IF(!q8 || !k8 || !vt8 || !q_scale || !k_scale || !v_scale || !o || !lse, FA_ERR_INVALID_ARG);
+  FA_REJECT_IF(!aligned16(q8) || !aligned16(k8) || !aligned16(vt8) || !aligned16(o) || !aligned4(lse) ||
+                   !aligned4(q_scale) || !aligned4(k_scale) || !aligned4(v_scale),
+               FA_ERR_INVALID_ARG);
+  FA_REJECT_IF(B < 1 || H < 1 || N < 1 || d < 1, FA_ERR_INVALID_ARG);
+  FA_REJECT_IF(!(scale > 0.f) || !std::isfinite(scale), FA_ERR_INVALID_ARG);
+  FA_REJECT_IF(causal != 0 && causal != 1, FA_ERR_INVALID_ARG);
+  FA_REJECT_IF(v_pitch < N || v_pitch % 16 != 0, FA_ERR_INVALID_ARG);
+  FA_REJECT_IF(d != 128, FA_ERR_UNSUPPORTED);
   const long long bh = static_cast<long long>(B) * H;
   const long long pairs = (static_cast<long long>(N) + 255) / 256;
-  if (bh > 0x7fffffffLL || pairs > 65535) return FA_ERR_INVALID_ARG;
+  FA_REJECT_IF(bh > 0x7fffffffLL || pairs > 65535, FA_ERR_INVALID_ARG);
   int dev = -1;
   fa_status st = current_device(&dev);
   if (st != FA_OK) return st;
@@ -443,16 +476,10 @@ fa_status fa_fwd_fp8(const void* q8, const void* k8, const void* vt8, const floa
 
 fa_status fa_decode(const void* q, const void* k_cache, const void* v_cache, const int32_t* seqlens, void* o,
                     float* lse, int B, int H, int L, int d, int num_splits, fa_stream_t stream) {
-  if (!q || !k_cache || !v_cache || !seqlens || !o || !lse) return FA_ERR_INVALID_ARG;
-  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned4(seqlens) || !aligned4(o) ||
-      !aligned4(lse))
-    return FA_ERR_INVALID_ARG;
-  if (B < 1 || H < 1 || L < 1 || d < 1) return FA_ERR_INVALID_ARG;
-  if (num_splits < 1 || num_splits > 64) return FA_ERR_INVALID_ARG;
-  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
-  if (static_cast<long long>(B) * H > 0x7fffffffLL || H > 65535 || B > 65535) return FA_ERR_INVALID_ARG;
+  fa_status st = check_decode_args(q, k_cache, v_cache, seqlens, o, lse, B, H, L, d, num_splits);
+  if (st != FA_OK) return st;
   int dev = -1;
-  fa_status st = current_device(&dev);
+  st = current_device(&dev);
   if (st != FA_OK) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const size_t parts = static_cast<size_t>(B) * H * num_splits;
@@ -473,16 +500,17 @@ fa_status fa_decode(const void* q, const void* k_cache, const void* v_cache, con
 
 fa_status fa_decode_gqa(const void* q, const void* k_cache, const void* v_cache, const int32_t* seqlens, void* o,
                         float* lse, int B, int Hq, int Hkv, int L, int d, int num_splits, fa_stream_t stream) {
-  if (!q || !k_cache || !v_cache || !seqlens || !o || !lse) return FA_ERR_INVALID_ARG;
-  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned4(seqlens) || !aligned4(o) ||
-      !aligned4(lse))
-    return FA_ERR_INVALID_ARG;
-  if (B < 1 || Hq < 1 || Hkv < 1 || L < 1 || d < 1 || Hq % Hkv != 0) return FA_ERR_INVALID_ARG;
-  if (num_splits < 1 || num_splits > 64) return FA_ERR_INVALID_ARG;
-  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  FA_REJECT_IF(!q || !k_cache || !v_cache || !seqlens || !o || !lse, FA_ERR_INVALID_ARG);
+  FA_REJECT_IF(!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned4(seqlens) || !aligned4(o) ||
+                   !aligned4(lse),
+               FA_ERR_INVALID_ARG);
+  FA_REJECT_IF(B < 1 || Hq < 1 || Hkv < 1 || L < 1 || d < 1 || Hq % Hkv != 0, FA_ERR_INVALID_ARG);
+  FA_REJECT_IF(num_splits < 1 || num_splits > 64, FA_ERR_INVALID_ARG);
+  FA_REJECT_IF(d != 64 && d != 128, FA_ERR_UNSUPPORTED);
   const long long groups = (Hq / Hkv + 15) / 16;
-  if (B > 65535 || static_cast<long long>(Hkv) * groups > 65535 || static_cast<long long>(B) * Hq > 0x7fffffffLL)
-    return FA_ERR_INVALID_ARG;
+  FA_REJECT_IF(B > 65535 || static_cast<long long>(Hkv) * groups > 65535 ||
+                   static_cast<long long>(B) * Hq > 0x7fffffffLL,
+               FA_ERR_INVALID_ARG);
   int dev = -1;
   fa_status st = current_device(&dev);
   if (st != FA_OK) return st;
@@ -508,16 +536,16 @@ fa_status fa_decode_gqa(const void* q, const void* k_cache, const void* v_cache,
 
 fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
                  void* dq, void* dk, void* dv, int B, int H, int N, int d, int causal, float scale, fa_stream_t stream) {
-  if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv) return FA_ERR_INVALID_ARG;
-  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned4(lse) || !aligned16(dout) ||
-      !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
-    return FA_ERR_INVALID_ARG;
-  if (B < 1 || H < 1 || N < 1 || d < 1) return FA_ERR_INVALID_ARG;
-  if (!(scale > 0.f) || !std::isfinite(scale)) return FA_ERR_INVALID_ARG;
-  if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
-  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  FA_REJECT_IF(!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv, FA_ERR_INVALID_ARG);
+  FA_REJECT_IF(!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned4(lse) ||
+                   !aligned16(dout) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv),
+               FA_ERR_INVALID_ARG);
+  FA_REJECT_IF(B < 1 || H < 1 || N < 1 || d < 1, FA_ERR_INVALID_ARG);
+  FA_REJECT_IF(!(scale > 0.f) || !std::isfinite(scale), FA_ERR_INVALID_ARG);
+  FA_REJECT_IF(causal != 0 && causal != 1, FA_ERR_INVALID_ARG);
+  FA_REJECT_IF(d != 64 && d != 128, FA_ERR_UNSUPPORTED);
   const long long bh = static_cast<long long>(B) * H;
-  if (bh > 0x7fffffffLL || (static_cast<long long>(N) + 127) / 128 > 65535) return FA_ERR_INVALID_ARG;
+  FA_REJECT_IF(bh > 0x7fffffffLL || (static_cast<long long>(N) + 127) / 128 > 65535, FA_ERR_INVALID_ARG);
   int dev = -1;
   fa_status st = current_device(&dev);
   if (st != FA_OK) return st;
@@ -541,7 +569,7 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
 }
 
 fa_status fa_bwd_plan(int N, int d, int block, int causal, long long* dq_atomic_adds) {
-  if (N < 1 || d < 1 || block < 1 || !dq_atomic_adds) return FA_ERR_INVALID_ARG;
+  FA_REJECT_IF(N < 1 || d < 1 || block < 1 || !dq_atomic_adds, FA_ERR_INVALID_ARG);
   const long long t = (static_cast<long long>(N) + block - 1) / block;
   long long adds = 0;
   for (long long j = 0; j < t; ++j) {
@@ -555,8 +583,8 @@ fa_status fa_bwd_plan(int N, int d, int block, int causal, long long* dq_atomic_
   return FA_OK;
 }
 
-fa_status fa_check_device_error(fa_stream_t stream, int* site) {
-  if (site) *site = 0;
+fa_status fa_check_device_error(fa_stream_t stream) {
+  t_error_site = 0;
   cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) {
     set_error_text("cudaStreamSynchronize", e);
@@ -571,13 +599,17 @@ fa_status fa_check_device_error(fa_stream_t stream, int* site) {
     set_error_text("reading the device error word", e);
     return FA_ERR_CUDA;
   }
-  if (site) *site = static_cast<int>(host[1]);
-  if (host[0] & kErrTimeout) return FA_ERR_TIMEOUT;
-  return (host[0] & kErrCheck) ? FA_ERR_CHECK : FA_OK;
+  if ((host[0] & (kErrTimeout | kErrCheck)) == 0) return FA_OK;
+  t_error_site = static_cast<int>(host[1]);
+  char buf[96];
+  std::snprintf(buf, sizeof(buf), "site %d (%s)", t_error_site,
+                (host[0] & kErrTimeout) ? "a bounded wait ran out" : "protocol check failed");
+  set_error_text("device error word", buf);
+  return (host[0] & kErrTimeout) ? FA_ERR_TIMEOUT : FA_ERR_CHECK;
 }
 
 fa_status fa_fwd_plan(int N, int block, int causal, long long* pairs_total, long long* pairs_computed) {
-  if (N < 1 || block < 1 || !pairs_total || !pairs_computed) return FA_ERR_INVALID_ARG;
+  FA_REJECT_IF(N < 1 || block < 1 || !pairs_total || !pairs_computed, FA_ERR_INVALID_ARG);
   const long long t = (static_cast<long long>(N) + block - 1) / block;
   long long done = 0;
   for (long long i = 0; i < t; ++i) done += fwd_kv_tiles(static_cast<int>(i * block), N, block, causal);
@@ -587,8 +619,8 @@ fa_status fa_fwd_plan(int N, int block, int causal, long long* pairs_total, long
 }
 
 fa_status fa_selftest_mma(int mode, const void* a, const void* b, float* d, int n, int k, fa_stream_t stream) {
-  if (!a || !b || !d || !aligned16(a) || !aligned16(b) || !aligned4(d)) return FA_ERR_INVALID_ARG;
-  if (mode < 0 || mode > 3) return FA_ERR_INVALID_ARG;
+  FA_REJECT_IF(!a || !b || !d || !aligned16(a) || !aligned16(b) || !aligned4(d), FA_ERR_INVALID_ARG);
+  FA_REJECT_IF(mode < 0 || mode > 3, FA_ERR_INVALID_ARG);
   int dev = -1;
   fa_status st = current_device(&dev);
   if (st != FA_OK) return st;
@@ -598,7 +630,7 @@ fa_status fa_selftest_mma(int mode, const void* a, const void* b, float* d, int 
 }
 
 fa_status fa_selftest_wait_timeout(unsigned int timeout_us, fa_stream_t stream) {
-  if (timeout_us == 0 || timeout_us > 5000000u) return FA_ERR_INVALID_ARG;
+  FA_REJECT_IF(timeout_us == 0 || timeout_us > 5000000u, FA_ERR_INVALID_ARG);
   int dev = -1;
   fa_status st = current_device(&dev);
   if (st != FA_OK) return st;

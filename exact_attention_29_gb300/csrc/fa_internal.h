@@ -26,6 +26,20 @@ bool encode_f32_map(CUtensorMap* map, const void* base, uint64_t d, uint64_t row
 void set_error_text(const char* what, cudaError_t err);
 void set_error_text(const char* what, const char* detail);
 
+// Record why a call was rejected (the failed check, as source text) and return `status`.
+fa_status reject(fa_status status, const char* failed_check);
+#define FA_REJECT_IF(cond, status)                  \
+  do {                                              \
+    if (cond) return ::fa::reject((status), #cond); \
+  } while (0)
+
+// The current device, checked to be compute capability 10.3 (FA_ERR_UNSUPPORTED otherwise).
+fa_status checked_device(int* dev);
+
+// Argument checks shared by fa_decode and fa_decode_noalloc (pointers, alignment, sizes, d, splits).
+fa_status check_decode_args(const void* q, const void* k_cache, const void* v_cache, const int32_t* seqlens,
+                            const void* o, const float* lse, int B, int H, int L, int d, int num_splits);
+
 // Device error word of the current device (see fa_common.cuh).
 unsigned int* device_error_word();
 

@@ -21,7 +21,10 @@
 //     ordering between them) race on the array and must not be issued;
 //   * the first call on each device looks up the array's device address
 //     (cudaGetSymbolAddress, with that device current) and caches it; make that
-//     first call before any stream capture.
+//     first call before any stream capture. The cached address belongs to the
+//     CUDA context of that moment: after cudaDeviceReset the library must not
+//     be used again in the process (fa_decode and the other calls cache the
+//     device error word's address the same way).
 #include <cuda_runtime.h>
 
 #include <cstdio>
@@ -68,8 +71,6 @@ fa_status workspace_ptr(float** out) {
   return FA_OK;
 }
 
-bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
-
 }  // namespace
 }  // namespace fa
 
@@ -77,14 +78,8 @@ extern "C" fa_status fa_decode_noalloc(const void* q, const void* k_cache, const
                                        const int32_t* seqlens, void* o, float* lse, int B, int H, int L, int d,
                                        int num_splits, fa_stream_t stream) {
   using namespace fa;
-  if (!q || !k_cache || !v_cache || !seqlens || !o || !lse) return FA_ERR_INVALID_ARG;
-  if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(seqlens, 4) ||
-      !aligned(o, 4) || !aligned(lse, 4))
-    return FA_ERR_INVALID_ARG;
-  if (B < 1 || H < 1 || L < 1 || d < 1) return FA_ERR_INVALID_ARG;
-  if (num_splits < 1 || num_splits > 64) return FA_ERR_INVALID_ARG;
-  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
-  if (static_cast<long long>(B) * H > 0x7fffffffLL || H > 65535 || B > 65535) return FA_ERR_INVALID_ARG;
+  fa_status st = check_decode_args(q, k_cache, v_cache, seqlens, o, lse, B, H, L, d, num_splits);
+  if (st != FA_OK) return st;
   const size_t parts = static_cast<size_t>(B) * H * num_splits;
   const size_t need = parts * (d + 1);
   if (need > kNoallocWorkspaceFloats) {
@@ -94,17 +89,11 @@ extern "C" fa_status fa_decode_noalloc(const void* q, const void* k_cache, const
     set_error_text("fa_decode_noalloc", buf);
     return FA_ERR_INVALID_ARG;
   }
-  int major = 0, minor = 0, dev = -1;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
-  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
-  if (e != cudaSuccess) {
-    set_error_text("device query", e);
-    return FA_ERR_CUDA;
-  }
-  if (major != 10 || minor != 3) return FA_ERR_UNSUPPORTED;
+  int dev = -1;
+  st = checked_device(&dev);
+  if (st != FA_OK) return st;
   float* ws = nullptr;
-  fa_status st = workspace_ptr(&ws);
+  st = workspace_ptr(&ws);
   if (st != FA_OK) return st;
   return launch_decode(q, k_cache, v_cache, seqlens, o, lse, B, H, L, d, num_splits, ws, ws + parts * d,
                        reinterpret_cast<cudaStream_t>(stream));

@@ -151,13 +151,17 @@ def decode_inputs(B: int, H: int, L: int, d: int, seed: int = 0, ragged: bool = 
     q = _randn_bf16((B, H, d), g, device)
     k = _randn_bf16((B, H, L, d), g, device)
     v = _randn_bf16((B, H, L, d), g, device)
-    if ragged:
-        gl = torch.Generator(device="cpu")
-        gl.manual_seed(seed + 1)
-        seqlens = torch.randint(min(lo, L), L + 1, (B,), generator=gl, dtype=torch.int64).to(torch.int32)
-    else:
-        seqlens = torch.full((B,), L, dtype=torch.int32)
-    return q, k, v, seqlens.to(device)
+    return q, k, v, decode_seqlens(B, L, seed, ragged, lo).to(device)
+
+
+def decode_seqlens(B: int, L: int, seed: int = 0, ragged: bool = False, lo: int = 1024) -> torch.Tensor:
+    """Cache lengths [B] (int32, on the host): all L, or (ragged) uniform
+    integers in [min(lo, L), L] from a generator seeded with ``seed + 1``."""
+    if not ragged:
+        return torch.full((B,), L, dtype=torch.int32)
+    gl = torch.Generator(device="cpu")
+    gl.manual_seed(seed + 1)
+    return torch.randint(min(lo, L), L + 1, (B,), generator=gl, dtype=torch.int64).to(torch.int32)
 
 
 def decode_gqa_inputs(B: int, Hq: int, Hkv: int, L: int, d: int, seed: int = 0, ragged: bool = False,
@@ -168,13 +172,7 @@ def decode_gqa_inputs(B: int, Hq: int, Hkv: int, L: int, d: int, seed: int = 0, 
     q = _randn_bf16((B, Hq, d), g, device)
     k = _randn_bf16((B, Hkv, L, d), g, device)
     v = _randn_bf16((B, Hkv, L, d), g, device)
-    if ragged:
-        gl = torch.Generator(device="cpu")
-        gl.manual_seed(seed + 1)
-        seqlens = torch.randint(min(lo, L), L + 1, (B,), generator=gl, dtype=torch.int64).to(torch.int32)
-    else:
-        seqlens = torch.full((B,), L, dtype=torch.int32)
-    return q, k, v, seqlens.to(device)
+    return q, k, v, decode_seqlens(B, L, seed, ragged, lo).to(device)
 
 
 def block_mask_bigbird(T: int, heads: int = 1, window: int = 1, globals_: int = 1, random: int = 2,

@@ -287,7 +287,14 @@ fa_status fa_decode_noalloc(const void *q, const void *k_cache, const void *v_ca
 /* Static text for a status code. Never NULL. */
 const char *fa_status_string(fa_status status);
 
-/* Text of the most recent FA_ERR_CUDA on the calling thread ("" if none). */
+/*
+ * Text of the reason for the most recent non-OK status returned on the calling
+ * thread ("" if there was none yet): the CUDA call that failed (FA_ERR_CUDA),
+ * the argument check that rejected a call (FA_ERR_INVALID_ARG,
+ * FA_ERR_UNSUPPORTED; for fa_decode_noalloc also the size of a request beyond
+ * its static workspace), or the device error word's site (FA_ERR_TIMEOUT,
+ * FA_ERR_CHECK). A later successful call leaves the text as it was.
+ */
 const char *fa_last_error_string(void);
 
 /*
@@ -296,10 +303,21 @@ const char *fa_last_error_string(void);
  * bounded waits ran out since the last check, FA_ERR_CHECK if (in a library
  * built with FA_DEBUG) a kernel's end-of-kernel protocol check failed: its
  * roles did not walk the same items, ring positions and barrier phases.
- * FA_ERR_CUDA if the stream reports an error, FA_OK otherwise. `site`, if not
- * NULL, receives the code of the first wait or check that failed (0 if none).
+ * FA_ERR_CUDA if the stream reports an error, FA_OK otherwise.
+ * The pages define no failure detection: the bounded waits this call reports
+ * are the library's own. fa_last_error_site() gives the code of the wait or
+ * check that failed.
  */
-fa_status fa_check_device_error(fa_stream_t stream, int *site);
+fa_status fa_check_device_error(fa_stream_t stream);
+
+/*
+ * Site code of the first wait or check that failed, as read by the most recent
+ * fa_check_device_error on the calling thread (0 if that call found none).
+ * Codes: 1 Q landed, 2 K/V landed, 3 K/V slot free, 4 S done, 5 P written,
+ * 6 O done, 7 teardown drain, 8 Q buffer free, 9 O read out, 20-22 FA_DEBUG
+ * protocol checks (forward, backward, GQA decode), 100 the timeout self-test.
+ */
+int fa_last_error_site(void);
 
 /*
  * Work plan of fa_fwd (host only, no device needed): with square tiles of

@@ -13,6 +13,7 @@ attention(q, k, v, causal, scale)            -> (o, lse), [B,H,N,d] inputs
 attention_rows(q_rows, q_pos, k, v, ...)     -> (o, lse, s, p) for one head
 decode(q, k_cache, v_cache, seqlens)         -> (o, lse), one query per (b, h)
 attention_bwd(q, k, v, dout, causal, scale)  -> (dq, dk, dv), [B,H,N,d] inputs
+set_threads(n)                               -> OpenMP thread count (timing only)
 
 Inputs may be numpy arrays or torch CPU tensors of any float dtype; they are
 widened to fp64 exactly (bf16 and fp32 values are representable in fp64), so
@@ -75,8 +76,17 @@ def _load():
             lib.oracle_decode_gqa.restype = ctypes.c_int
             lib.oracle_attention_bwd.argtypes = [dp] * 7 + [ctypes.c_int] * 5 + [ctypes.c_double]
             lib.oracle_attention_bwd.restype = ctypes.c_int
+            lib.oracle_set_threads.argtypes = [ctypes.c_int]
+            lib.oracle_set_threads.restype = ctypes.c_int
             _lib = lib
     return _lib
+
+
+def set_threads(n: int) -> int:
+    """Thread count of the oracle's OpenMP loops for later calls from this
+    thread (timing only: results do not depend on it); returns the count in
+    effect. set_threads(0) leaves it unchanged and only reports it."""
+    return _load().oracle_set_threads(int(n))
 
 
 def _f64(x) -> np.ndarray:

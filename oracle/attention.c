@@ -41,6 +41,9 @@
 #include <math.h>
 #include <stdlib.h>
 #include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
 
 #define ORACLE_OK 0
 #define ORACLE_ERR_ARG 1
@@ -138,6 +141,22 @@ int oracle_attention_rows(const double *q, const int *q_pos, const double *k,
   if (p_out) memcpy(p_out, P, nn * sizeof(double));
   free(S); free(P); free(m); free(l);
   return ORACLE_OK;
+}
+
+/*
+ * Thread count of the OpenMP loops of later calls made from the calling
+ * thread (n >= 1); returns the count now in effect. Used to time the oracle
+ * on one core. Every row is computed by one thread in a fixed order, so the
+ * results do not depend on it.
+ */
+int oracle_set_threads(int n) {
+#ifdef _OPENMP
+  if (n >= 1) omp_set_num_threads(n);
+  return omp_get_max_threads();
+#else
+  (void)n;
+  return 1;
+#endif
 }
 
 /*

@@ -53,6 +53,43 @@ def compare(o_gpu, lse_gpu, o_ref, lse_ref, what=""):
     return do.max(), do.mean(), dl.max()
 
 
+class Accumulator:
+    """compare() over an output checked piece by piece (a head at a time): the
+    same bounds, with the maximum and the mean taken over every element added."""
+
+    def __init__(self, what: str):
+        self.what = what
+        self.max_do = 0.0
+        self.sum_do = 0.0
+        self.max_dl = 0.0
+        self.n_o = 0
+        self.n_lse = 0
+
+    def add(self, o_gpu, lse_gpu, o_ref, lse_ref):
+        o = o_gpu.float().cpu().numpy().astype(np.float64)
+        lse = lse_gpu.float().cpu().numpy().astype(np.float64)
+        assert o.shape == o_ref.shape and lse.shape == lse_ref.shape, self.what
+        finite = bool(np.all(np.isfinite(o)) and np.all(np.isfinite(lse)))
+        if not finite:
+            record("forward", self.what, False, elements=self.n_o + o.size)
+        assert finite, f"{self.what}: non-finite output"
+        do = np.abs(o - o_ref)
+        self.max_do = max(self.max_do, float(do.max()))
+        self.sum_do += float(do.sum())
+        self.max_dl = max(self.max_dl, float(np.abs(lse - lse_ref).max()))
+        self.n_o += o.size
+        self.n_lse += lse.size
+
+    def finish(self):
+        mean = self.sum_do / max(1, self.n_o)
+        ok = self.max_do <= MAX_ABS_O and mean <= MEAN_ABS_O and self.max_dl <= MAX_ABS_LSE
+        record("forward", self.what, ok, max_abs_dO=self.max_do, mean_abs_dO=mean, max_abs_dLSE=self.max_dl,
+               elements=self.n_o, lse_elements=self.n_lse)
+        assert ok, (f"{self.what}: max|dO|={self.max_do:.3e} mean|dO|={mean:.3e} max|dLSE|={self.max_dl:.3e} "
+                    f"over {self.n_o} elements")
+        return self.max_do, mean, self.max_dl
+
+
 def require_gpu():
     import torch
 

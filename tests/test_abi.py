@@ -26,13 +26,16 @@ def lib():
 def _declared_functions():
     text = open(HEADER).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return re.findall(r"^\s*(?:fa_status|const\s+char\s*\*)\s*\*?\s*(fa_\w+)\s*\(", text, flags=re.M)
+    return re.findall(r"^\s*(?:fa_status|int|const\s+char\s*\*)\s*\*?\s*(fa_\w+)\s*\(", text, flags=re.M)
 
 
 def test_header_declares_the_boundary():
     names = _declared_functions()
-    for required in ("fa_fwd", "fa_decode", "fa_status_string", "fa_check_device_error"):
+    for required in ("fa_fwd", "fa_decode", "fa_status_string", "fa_check_device_error", "fa_last_error_site"):
         assert required in names
+    # the error check takes the stream alone; the failing site has a call of its own
+    text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    assert re.search(r"fa_status\s+fa_check_device_error\s*\(\s*fa_stream_t\s+stream\s*\)\s*;", text)
 
 
 def test_every_declared_symbol_is_exported(lib):
@@ -101,18 +104,52 @@ def test_host_buffer_binding_rejects_device_or_strided_tensors():
         fa.fa_fwd_host(q, q, q, o=torch.zeros(1, 1, 8, 64), lse=torch.zeros(1, 1, 8))
 
 
-def test_decode_rejects_bad_arguments(lib):
+@pytest.mark.parametrize("entry", ["fa_decode", "fa_decode_noalloc"])
+def test_decode_rejects_bad_arguments(lib, entry):
+    """Both decode entry points run the same checks, before any CUDA call, and
+    leave the failed check's text for fa_last_error_string."""
     import exact_attention_29_gb300 as fa
 
-    def dec(num_splits=8, d=128, L=64, seqlens=16, q=16):
-        return lib.fa_decode(q, 16, 16, seqlens, 16, 16, 1, 1, L, d, num_splits, None)
+    call = getattr(lib, entry)
+
+    def dec(num_splits=8, d=128, L=64, seqlens=16, q=16, B=1, H=1):
+        return call(q, 16, 16, seqlens, 16, 16, B, H, L, d, num_splits, None)
 
     assert dec(num_splits=0) == fa.FA_ERR_INVALID_ARG
+    assert b"num_splits" in lib.fa_last_error_string()
     assert dec(num_splits=65) == fa.FA_ERR_INVALID_ARG
     assert dec(seqlens=None) == fa.FA_ERR_INVALID_ARG
+    assert b"seqlens" in lib.fa_last_error_string()
     assert dec(q=8) == fa.FA_ERR_INVALID_ARG
+    assert b"aligned16(q)" in lib.fa_last_error_string()
     assert dec(L=0) == fa.FA_ERR_INVALID_ARG
+    assert dec(B=70000) == fa.FA_ERR_INVALID_ARG
     assert dec(d=80) == fa.FA_ERR_UNSUPPORTED
+    assert b"d != 64" in lib.fa_last_error_string()
+
+
+def test_noalloc_size_limit_is_checked_on_the_host(lib):
+    """16 * 32 * 64 * 129 fp32 values exceed the 4,194,304 of the static array:
+    rejected before any CUDA call, with the sizes in the text."""
+    import exact_attention_29_gb300 as fa
+
+    st = lib.fa_decode_noalloc(16, 16, 16, 16, 16, 16, 16, 32, 64, 128, 64, None)
+    assert st == fa.FA_ERR_INVALID_ARG
+    assert b"static workspace" in lib.fa_last_error_string()
+
+
+def test_every_rejection_says_why(lib):
+    """A rejected call always leaves its reason, not an earlier call's text."""
+    import exact_attention_29_gb300 as fa
+
+    assert lib.fa_decode_noalloc(16, 16, 16, 16, 16, 16, 16, 32, 64, 128, 64, None) == fa.FA_ERR_INVALID_ARG
+    assert _fwd(lib, causal=2) == fa.FA_ERR_INVALID_ARG
+    assert b"causal" in lib.fa_last_error_string()
+    assert lib.fa_bwd_plan(0, 64, 128, 0, None) == fa.FA_ERR_INVALID_ARG
+    assert b"N < 1" in lib.fa_last_error_string()
+    assert lib.fa_selftest_wait_timeout(0, None) == fa.FA_ERR_INVALID_ARG
+    assert b"timeout_us" in lib.fa_last_error_string()
+    assert lib.fa_last_error_site() == 0
 
 
 def test_selftests_reject_bad_arguments(lib):

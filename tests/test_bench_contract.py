@@ -49,3 +49,29 @@ def test_peaks_are_read():
 
     peaks = bench._peaks()
     assert peaks["hbm_gbs"] > 1000 and peaks["bf16_tflops"] > 500
+
+
+def test_one_core_oracle_leg_restores_the_thread_count():
+    import bench
+    import oracle
+
+    before = oracle.set_threads(0)
+    out = bench.oracle_one_core()
+    assert set(out) == {"C1_pr1", "C2a_gpt2_small", "C2b_gpt2_small_causal"}
+    assert all(v["value"] > 0 and v["seconds"] > 0 and v["sample"] for v in out.values())
+    assert oracle.set_threads(0) == before
+
+
+def test_clock_windows():
+    """Each leg's clocks come from the samples inside its own host time window
+    (the nearest one when the window is shorter than the sampling period)."""
+    import bench
+
+    s = bench.ClockSampler("0")
+    idle = ["1000", "2070", "100", "0x0", "Not Active", "Not Active", "Not Active", "Not Active"]
+    busy = ["2070", "2070", "900", "0x0", "Not Active", "Not Active", "Not Active", "Active"]
+    s.rows = [(10.0, idle), (10.2, busy), (10.4, busy), (10.6, idle), (20.0, idle)]
+    w = s.summary(10.15, 10.45)
+    assert w["sm_mhz"] == 2070 and w["samples"] == 2 and w["reasons"] == ["sw_power_cap"]
+    near = s.summary(19.9, 19.95)
+    assert near["samples"] == 1 and near["sm_mhz"] == 1000 and near["reasons"] == []

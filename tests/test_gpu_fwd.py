@@ -5,7 +5,7 @@ import torch
 
 import oracle
 from exact_attention_29_gb300 import workloads as wl
-from parity import compare, require_gpu
+from parity import Accumulator, compare, require_gpu
 
 pytestmark = pytest.mark.gpu
 
@@ -89,12 +89,29 @@ def _sampled_check(c, rows_per_head, heads=None, seed=0):
     return o, lse
 
 
-def test_llama3_8b_prefill_sampled():
-    _sampled_check(wl.PREFILL["llama3_8b_prefill"], rows_per_head=64)
+def _full_check(c, seed=0):
+    """Full-size run on the GPU, then every row of every head against the oracle,
+    one head at a time (each head's S and P are N x N in fp64)."""
+    q, k, v = wl.prefill_inputs(c.B, c.H, c.N, c.d, seed=seed, device="cuda")
+    o, lse = _run(q, k, v, c.causal)
+    acc = Accumulator(f"{c.name} (all {c.B * c.H} heads, every row)")
+    pos = np.arange(c.N)
+    for b in range(c.B):
+        qb, kb, vb, ob, lb = q[b].cpu(), k[b].cpu(), v[b].cpu(), o[b].cpu(), lse[b].cpu()
+        for h in range(c.H):
+            o_ref, lse_ref, _, _ = oracle.attention_rows(qb[h], pos, kb[h], vb[h], c.causal, c.scale)
+            acc.add(ob[h], lb[h], o_ref, lse_ref)
+    acc.finish()
+    assert acc.n_o == c.B * c.H * c.N * c.d
 
 
-def test_llama3_8b_prefill_noncausal_sampled():
-    _sampled_check(wl.PREFILL["llama3_8b_prefill_noncausal"], rows_per_head=32)
+def test_llama3_8b_prefill_full_oracle():
+    """B2 H32 N4096 d128 causal: the whole output (33.5 M values of O, 262,144 of LSE)."""
+    _full_check(wl.PREFILL["llama3_8b_prefill"])
+
+
+def test_llama3_8b_prefill_noncausal_full_oracle():
+    _full_check(wl.PREFILL["llama3_8b_prefill_noncausal"])
 
 
 def test_long_16k_sampled():

@@ -77,6 +77,7 @@ def test_bounded_wait_times_out_and_context_survives():
     with pytest.raises(fa.FaError) as exc:
         fa.fa_check_device_error()
     assert exc.value.status == fa.FA_ERR_TIMEOUT and exc.value.site == 100
-    assert fa.fa_check_device_error() == 0
+    assert fa.fa_last_error_site() == 100 and "site 100" in str(exc.value)
+    assert fa.fa_check_device_error() == 0 and fa.fa_last_error_site() == 0
     x = torch.ones(1024, device="cuda")
     assert float(x.sum().item()) == 1024.0

@@ -4,15 +4,17 @@ nearly all of HBM, or a latency-critical decode loop). Its split partials live
 in a fixed 16 MiB array inside libfa.so instead of a per-call allocation.
 
 This file is collected last on purpose. Each check calls the new entry point
-through the C ABI and compares it with fa_decode on the same inputs, twice in
-a row, since all calls share one workspace that keeps the previous contents.
+through the C ABI and compares it with fa_decode and with the fp64 oracle on
+the same inputs, twice in a row, since all calls share one workspace that keeps
+the previous contents.
 """
 
 import pytest
 import torch
 
+import oracle
 from exact_attention_29_gb300 import workloads as wl
-from parity import MAX_ABS_LSE, MAX_ABS_O, MEAN_ABS_O, require_gpu
+from parity import MAX_ABS_LSE, MAX_ABS_O, MEAN_ABS_O, compare, require_gpu
 
 pytestmark = pytest.mark.gpu
 
@@ -22,6 +24,7 @@ WORKSPACE_FLOATS = 1 << 22
 @pytest.fixture(scope="module", autouse=True)
 def _gpu():
     require_gpu()
+    oracle.build()
 
 
 def _c_noalloc(lib, q, kc, vc, sl, splits, o, lse):
@@ -58,11 +61,13 @@ def test_noalloc_matches_decode_on_two_calls_in_a_row():
         torch.cuda.synchronize()
         fa.fa_check_device_error()
         _close(o, lse, o_ref, lse_ref)
+        ro, rl = oracle.decode(q.cpu(), kc.cpu(), vc.cpu(), sl.cpu())
+        compare(o, lse, ro, rl, f"fa_decode_noalloc B{B} H{H} L{L} d{d} S{splits}")
 
 
 def test_noalloc_allocates_nothing():
     """After the first call on the device (which looks up the workspace address),
-    further calls leave the device's free memory unchanged."""
+    further calls leave the device's free memory and torch's allocator unchanged."""
     import exact_attention_29_gb300 as fa
 
     lib = fa.load_library()
@@ -73,10 +78,14 @@ def test_noalloc_allocates_nothing():
     assert _c_noalloc(lib, q, kc, vc, sl, 32, o, lse) == fa.FA_OK
     torch.cuda.synchronize()
     free_before = torch.cuda.mem_get_info()[0]
+    torch_before = (torch.cuda.memory_allocated(), torch.cuda.memory_reserved())
     for _ in range(2):
         assert _c_noalloc(lib, q, kc, vc, sl, 32, o, lse) == fa.FA_OK
     torch.cuda.synchronize()
+    assert (torch.cuda.memory_allocated(), torch.cuda.memory_reserved()) == torch_before
     assert torch.cuda.mem_get_info()[0] >= free_before
+    ro, rl = oracle.decode(q.cpu(), kc.cpu(), vc.cpu(), sl.cpu())
+    compare(o, lse, ro, rl, "fa_decode_noalloc after repeated calls")
     o_ref, lse_ref = fa.fa_decode(q, kc, vc, sl, 32)
     _close(o, lse, o_ref, lse_ref)
 
