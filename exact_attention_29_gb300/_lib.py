@@ -474,7 +474,10 @@ def fa_fwd_plan(N: int, block: int = 128, causal: bool = False):
 
 def fa_selftest_mma(mode: int, a: torch.Tensor, b: torch.Tensor, n: int, k: int, stream=None) -> torch.Tensor:
     lib = load_library()
-    d = torch.empty((128, n), dtype=torch.float32, device=a.device)
+    if mode in (4, 5):  # a CTA pair: 256 rows of D, then the two CTAs' TMEM base addresses
+        d = torch.empty((256 * n + 2,), dtype=torch.float32, device=a.device)
+    else:
+        d = torch.empty((128, n), dtype=torch.float32, device=a.device)
     _same_device(a.device, b=b)
     _check(lib.fa_selftest_mma(mode, a.data_ptr(), b.data_ptr(), d.data_ptr(), n, k, _stream_handle(stream)),
            "fa_selftest_mma")

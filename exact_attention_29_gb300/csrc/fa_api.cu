@@ -620,7 +620,7 @@ fa_status fa_fwd_plan(int N, int block, int causal, long long* pairs_total, long
 
 fa_status fa_selftest_mma(int mode, const void* a, const void* b, float* d, int n, int k, fa_stream_t stream) {
   FA_REJECT_IF(!a || !b || !d || !aligned16(a) || !aligned16(b) || !aligned4(d), FA_ERR_INVALID_ARG);
-  FA_REJECT_IF(mode < 0 || mode > 3, FA_ERR_INVALID_ARG);
+  FA_REJECT_IF(mode < 0 || mode > 5, FA_ERR_INVALID_ARG);
   int dev = -1;
   fa_status st = current_device(&dev);
   if (st != FA_OK) return st;

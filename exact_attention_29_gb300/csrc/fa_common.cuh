@@ -64,6 +64,25 @@ __device__ __forceinline__ bool bounded_wait(uint64_t* bar, uint32_t parity, vol
   }
 }
 
+// bounded_wait for a barrier that also receives arrivals from the peer CTA of a
+// pair: the wait acquires at cluster scope, so the peer's writes released by
+// its arrival are visible afterwards.
+__device__ __forceinline__ bool bounded_wait_cluster(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                                     unsigned int* err, int site,
+                                                     uint64_t timeout_ns = kWaitTimeoutNs) {
+  if (mbar_try_wait_cluster(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (;;) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    if (abort_flag != nullptr && *abort_flag) return false;
+    if (globaltimer_ns() - t0 > timeout_ns) {
+      if (abort_flag != nullptr) *abort_flag = 1;
+      record_timeout(err, site);
+      return false;
+    }
+  }
+}
+
 // Number of K/V tiles a Q tile starting at row `q_start` visits, with square
 // tiles of `block` rows: all of them without a mask; under the causal mask
 // only those not entirely above the diagonal, i.e. tiles 0 .. last_row/block

@@ -196,6 +196,125 @@ fa_status launch_mma_f8(int mode, const void* a, const void* b, float* d, cudaSt
   return FA_OK;
 }
 
+// Products of a CTA pair (M = 256, tcgen05 .cta_group::2), both operands in
+// shared memory; CTA r holds rows [128r, 128r + 128) of A and receives the
+// same rows of D:
+//   mode 4: D[256][128] = A[256][128] * B[128][128]^T, B K-major, CTA r holds
+//           B rows [64r, 64r + 64) (the S = Q K^T product of the pair kernel);
+//   mode 5: D[256][128] = A[256][128] * B[128][128], B MN-major, CTA r holds B
+//           columns [64r, 64r + 64) (the O += P V product with P in shared memory).
+// d also receives, after the 256 x 128 values, each CTA's TMEM base address.
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(128, 1)
+    pair_mma_test_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
+                         float* __restrict__ d, int mode, unsigned int* err) {
+  extern __shared__ uint8_t raw[];
+  uint8_t* base = raw + ((1024u - (smem_u32(raw) & 1023u)) & 1023u);
+  uint8_t* sa = base;                    // 2 chunks of 128 rows x 128 B
+  uint8_t* sb = base + 2 * kChunkBytes;  // mode 4: 2 chunks of 64 rows; mode 5: 1 chunk of 128 rows
+  uint64_t* bars = reinterpret_cast<uint64_t*>(base + 3 * kChunkBytes);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 4);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  if (threadIdx.x == 0) {
+    mbar_init(&bars[0], 1);  // this CTA's operands landed
+    mbar_init(&bars[1], 1);  // the pair's product is done (commit to both CTAs)
+    mbar_init(&bars[2], 2);  // even CTA: both CTAs' operands landed
+    fence_barrier_init();
+  }
+  cluster_sync();
+  if (warp == 0) {
+    tmem_alloc_pair(tmem_slot, 256);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+  if (threadIdx.x == 0) {
+    mbar_arrive_expect_tx(&bars[0], 3 * kChunkBytes);
+    for (int c = 0; c < 2; ++c)
+      tma_load_3d(sa + c * kChunkBytes, &tm_a, &bars[0], c * 64, 128 * static_cast<int>(rank), 0);
+    if (mode == 4) {
+      for (int c = 0; c < 2; ++c)
+        tma_load_3d(sb + c * (kChunkBytes / 2), &tm_b, &bars[0], c * 64, 64 * static_cast<int>(rank), 0);
+    } else {
+      tma_load_3d(sb, &tm_b, &bars[0], 64 * static_cast<int>(rank), 0, 0);
+    }
+    bounded_wait(&bars[0], 0, nullptr, err, kSiteSelftest);
+    mbar_arrive_cluster(mapa_shared(&bars[2], 0));
+    if (rank == 0) {
+      const bool ok = bounded_wait_cluster(&bars[2], 0, nullptr, err, kSiteSelftest);
+      if (ok) {
+        tc_fence_after();
+        const uint64_t ad = smem_desc_sw128(smem_u32(sa), 16, 1024);
+        if (mode == 4) {
+          constexpr uint32_t idesc = idesc_bf16_f32(256, 128, false, false);
+          const uint64_t bd = smem_desc_sw128(smem_u32(sb), 16, 1024);
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint32_t k32 = static_cast<uint32_t>((kk % 4) * 32);
+            umma_ss_pair(tmem, ad + desc_step((kk / 4) * kChunkBytes + k32),
+                         bd + desc_step((kk / 4) * (kChunkBytes / 2) + k32), idesc, kk > 0 ? 1u : 0u);
+          }
+        } else {
+          constexpr uint32_t idesc = idesc_bf16_f32(256, 128, false, true);
+          const uint64_t bd = smem_desc_sw128(smem_u32(sb), kChunkBytes, 1024);
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            umma_ss_pair(tmem, ad + desc_step((kk / 4) * kChunkBytes + (kk % 4) * 32), bd + desc_step(kk * 2048),
+                         idesc, kk > 0 ? 1u : 0u);
+        }
+      }
+      umma_commit_pair(&bars[1]);
+    }
+  }
+  __syncwarp();
+  const bool done = bounded_wait(&bars[1], 0, nullptr, err, kSiteSelftest);
+  if (__all_sync(0xffffffffu, done)) {
+    tc_fence_after();
+    const int row = 128 * static_cast<int>(rank) + warp * 32 + lane;
+#pragma unroll 1
+    for (int c = 0; c < 128; c += 32) {
+      uint32_t r[32];
+      tmem_ld_x32(tmem + lane_base + c, r);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) d[static_cast<size_t>(row) * 128 + c + i] = __uint_as_float(r[i]);
+    }
+  }
+  if (threadIdx.x == 0) d[256 * 128 + rank] = __uint_as_float(tmem);
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();
+  if (warp == 0) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc_pair(tmem, 256);
+  }
+  cluster_sync();
+}
+
+fa_status launch_pair_mma(int mode, const void* a, const void* b, float* d, cudaStream_t stream, unsigned int* err) {
+  CUtensorMap ta, tb;
+  // A [256][128] K-major, 128-row boxes; B [128][128]: K-major 64-row boxes (mode 4)
+  // or MN-major (rows = contraction index) 128-row boxes of 64 columns (mode 5)
+  if (!encode_bf16_map(&ta, a, 128, 256, 1, 128) || !encode_bf16_map(&tb, b, 128, 128, 1, mode == 4 ? 64 : 128))
+    return FA_ERR_CUDA;
+  constexpr int smem = 3 * kChunkBytes + 64 + 1024;
+  cudaError_t e = cudaFuncSetAttribute(pair_mma_test_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) {
+    set_error_text("cudaFuncSetAttribute(pair_mma_test_kernel)", e);
+    return FA_ERR_CUDA;
+  }
+  pair_mma_test_kernel<<<2, 128, smem, stream>>>(ta, tb, d, mode, err);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) {
+    set_error_text("pair_mma_test_kernel launch", e);
+    return FA_ERR_CUDA;
+  }
+  return FA_OK;
+}
+
 __global__ void wait_test_kernel(unsigned int* err, unsigned long long timeout_ns) {
   __shared__ uint64_t bar;
   if (threadIdx.x == 0) {
@@ -241,6 +360,7 @@ fa_status launch_selftest_mma(int mode, const void* a, const void* b, float* d, 
   if (mode == 1 && n == 128 && k == 128) return launch_mma<128, 128>(1, a, b, d, stream, err);
   if (mode == 1 && n == 64 && k == 128) return launch_mma<128, 64>(1, a, b, d, stream, err);
   if ((mode == 2 || mode == 3) && n == 128 && k == 128) return launch_mma_f8(mode, a, b, d, stream, err);
+  if ((mode == 4 || mode == 5) && n == 128 && k == 128) return launch_pair_mma(mode, a, b, d, stream, err);
   return FA_ERR_UNSUPPORTED;
 }
 

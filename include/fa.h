@@ -343,8 +343,15 @@ fa_status fa_fwd_plan(int N, int block, int causal, long long *pairs_total, long
  *   mode 3: D = A * B^T with A placed in tensor memory as four e4m3 per 32-bit
  *           column and B [n][k] K-major in shared memory (the O += P V product
  *           with V given transposed), n = k = 128.
- *   a, b: bf16 (modes 0, 1) or e4m3 byte (modes 2, 3) device pointers;
- *   d: fp32 device pointer [128][n].
+ *   mode 4: a pair of CTAs (a cluster of two on two SMs) computes one
+ *           M = 256 product with tcgen05 .cta_group::2: D[256][128] =
+ *           A[256][128] * B[128][128]^T, B K-major; each CTA holds 128 rows of
+ *           A and 64 rows of B and receives its 128 rows of D.
+ *   mode 5: as mode 4 with B[128][128] MN-major (rows are the contraction
+ *           index), each CTA holding 64 of its columns.
+ *   a, b: bf16 (modes 0, 1, 4, 5) or e4m3 byte (modes 2, 3) device pointers;
+ *   d: fp32 device pointer [128][n] (modes 4, 5: [256][128] followed by the
+ *   two CTAs' TMEM base addresses, 2 more 32-bit values).
  *
  * fa_selftest_wait_timeout: launch one block that waits on a barrier nothing
  *   ever arrives at, bounded by `timeout_us`; the kernel gives up, records

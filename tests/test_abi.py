@@ -157,7 +157,7 @@ def test_selftests_reject_bad_arguments(lib):
 
     assert lib.fa_selftest_wait_timeout(0, None) == fa.FA_ERR_INVALID_ARG
     assert lib.fa_selftest_wait_timeout(10_000_000, None) == fa.FA_ERR_INVALID_ARG
-    assert lib.fa_selftest_mma(4, 16, 16, 16, 128, 128, None) == fa.FA_ERR_INVALID_ARG
+    assert lib.fa_selftest_mma(6, 16, 16, 16, 128, 128, None) == fa.FA_ERR_INVALID_ARG
     assert lib.fa_selftest_mma(-1, 16, 16, 16, 128, 128, None) == fa.FA_ERR_INVALID_ARG
 
 

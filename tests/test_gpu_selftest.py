@@ -67,6 +67,26 @@ def test_mma_e4m3(mode):
     assert err <= 1e-6 * ref.abs().max().item() + 1e-3, err
 
 
+@pytest.mark.parametrize("mode", [4, 5])
+def test_mma_cta_pair(mode):
+    """A cluster of two CTAs computes one M = 256 product (tcgen05 .cta_group::2):
+    mode 4 D = A B^T with B K-major (S = Q K^T), mode 5 D = A B with B MN-major
+    (O += P V with P in shared memory). Each CTA holds half of B and gets its
+    128 rows of D; both see the same TMEM base address."""
+    import exact_attention_29_gb300 as fa
+
+    a, b = _rand((256, 128), 11 + mode), _rand((128, 128), 13 + mode)
+    out = fa.fa_selftest_mma(mode, a.cuda(), b.cuda(), 128, 128)
+    fa.fa_check_device_error()
+    out = out.cpu()
+    d = out[: 256 * 128].reshape(256, 128).double()
+    bases = out[256 * 128:].view(torch.int32).tolist()
+    ref = a.double() @ (b.double().T if mode == 4 else b.double())
+    err = (d - ref).abs().max().item()
+    assert err <= 1e-3, (err, bases)
+    assert bases[0] == bases[1], bases
+
+
 def test_bounded_wait_times_out_and_context_survives():
     """A wait on a barrier nothing arrives at gives up after its limit, the host
     reads FA_ERR_TIMEOUT, the word is cleared, and the GPU keeps working."""
