@@ -378,7 +378,7 @@ fa_status fa_fwd_sparse(const void* q, const void* k, const void* v, const uint8
   const size_t tiles = (static_cast<size_t>(N) + 127) / 128;
   const size_t rows = static_cast<size_t>(mask_heads) * ((static_cast<size_t>(N) + 255) / 256);
   void* ws = nullptr;
-  st = ws_alloc(dev, &ws, rows * tiles * sizeof(uint32_t) + rows * sizeof(int), s,
+  st = ws_alloc(dev, &ws, rows * tiles * sizeof(uint32_t) + 3 * rows * sizeof(int), s,
                 "workspace allocation (block-sparse step lists)");
   if (st != FA_OK) return st;
   cudaError_t e = cudaSuccess;
@@ -405,14 +405,8 @@ fa_status fa_fwd_sparse_plan(const uint8_t* mask, int mask_heads, int B, int H, 
     auto ok = [&](int i, int j) { return (!causal || j <= i) && mk[static_cast<size_t>(i) * T + j] != 0; };
     for (int i = 0; i < T; ++i)
       for (int j = 0; j < T; ++j) allowed += ok(i, j) ? 1 : 0;
-    // the kernel walks, for each pair of Q tiles, the union of their K/V tiles
-    // (at least one step, fully masked when the union is empty)
-    for (int i0 = 0; i0 < T; i0 += 2) {
-      const bool has1 = i0 + 1 < T;
-      long long nu = 0;
-      for (int j = 0; j < T; ++j) nu += (ok(i0, j) || (has1 && ok(i0 + 1, j))) ? 1 : 0;
-      computed += (nu > 0 ? nu : 1) * (has1 ? 2 : 1);
-    }
+    // each Q tile computes exactly the (Q tile, K/V tile) pairs its mask keeps
+    computed = allowed;
   }
   *pairs_allowed = allowed * B;
   *pairs_computed = computed * B;

@@ -31,9 +31,9 @@
 //   tensor core works on tile 1's products, and the other way round.
 //
 // With a block mask (block-sparse FlashAttention, "FlashAttention 完全拆解
-// （一）", block-sparse extension) an item's two Q tiles walk the union of
-// the K/V tiles their masks keep; tiles outside the union are never loaded or
-// multiplied.
+// （一）", block-sparse extension) an item's two Q tiles share the copies of
+// the union of the K/V tiles their masks keep, and each Q tile computes only
+// the K/V tiles its own mask keeps; tiles outside the union are never loaded.
 //
 // The same kernel runs the FP8 path ("已有的几种大模型上下文支持情况" §4.4,
 // FA-3): e4m3 Q and K with one scale per 128-row tile (the product of the two
@@ -96,7 +96,8 @@ struct FwdParams {
   // block-sparse mode only: per (mask head, Q-tile pair) the union of the K/V
   // tiles its two Q tiles keep, as words (tile | allowed for Q tile 0 << 16 |
   // allowed for Q tile 1 << 17), list[(mh * pairs + pair) * tiles + step], and
-  // the step counts cnt[mh * pairs + pair] (>= 1)
+  // cnt[3 * (mh * pairs + pair) + {0, 1, 2}]: the union's step count and the
+  // number of those steps Q tile 0 and Q tile 1 keep
   const uint32_t* list;
   const int* cnt;
   int mask_heads;
@@ -155,18 +156,20 @@ __device__ __forceinline__ Smem carve(uint8_t* raw) {
 
 // One work item: Q rows [q0, q0 + 256) of head bh; tile t visits n(t) K/V tiles.
 // Dense: tile t visits K/V tiles 0 .. n(t)-1. Block-sparse ("FlashAttention
-// 完全拆解（一）", block-sparse extension): both tiles walk the union of the
-// K/V tiles their masks keep (sparse_list_kernel), a step that one tile's
-// mask removes being fully masked for that tile; an item whose union is empty
-// walks tile 0 fully masked, so its rows still get o = 0, lse = -inf.
+// 完全拆解（一）", block-sparse extension): the item walks the union of the
+// K/V tiles the two tiles' masks keep (sparse_list_kernel), and tile t computes
+// the kept(t) steps its own mask keeps; a tile that keeps none writes o = 0 and
+// lse = -inf for its rows.
 struct Item {
   int bh;
   int q0;
   int r0, r1;  // first query row of tile 0 and of tile 1
   int n0;
   int n1;
+  int c0, c1;            // steps tile 0 and tile 1 compute (block-sparse: the steps their masks keep)
   const uint32_t* list;  // block-sparse: this item's steps
   __device__ __forceinline__ int n(int t) const { return t ? n1 : n0; }
+  __device__ __forceinline__ int kept(int t) const { return t ? c1 : c0; }
   __device__ __forceinline__ int row(int t) const { return t ? r1 : r0; }
   __device__ __forceinline__ int n_max() const { return n0 > n1 ? n0 : n1; }
 };
@@ -196,16 +199,20 @@ __device__ __forceinline__ bool item_at(const FwdParams& p, int k, Item& it) {
     it.r1 = p.swap_tiles ? it.q0 : it.q0 + kBM;
     it.n0 = fwd_kv_tiles(it.r0, p.N, kBN, p.causal);
     it.n1 = fwd_kv_tiles(it.r1, p.N, kBN, p.causal);
+    it.c0 = it.n0;
+    it.c1 = it.n1;
     it.list = nullptr;
   } else {
     const int mh = (p.mask_heads == 1) ? 0 : (it.bh % p.H);
     const size_t row = static_cast<size_t>(mh) * p.num_pairs + pair;
-    const int nu = __ldg(p.cnt + row);
+    const int nu = __ldg(p.cnt + 3 * row);
     it.r0 = it.q0;
     it.r1 = it.q0 + kBM;
     it.list = p.list + row * p.tiles;
     it.n0 = nu;
     it.n1 = (it.q0 + kBM < p.N) ? nu : 0;
+    it.c0 = __ldg(p.cnt + 3 * row + 1);
+    it.c1 = (it.q0 + kBM < p.N) ? __ldg(p.cnt + 3 * row + 2) : 0;
   }
   return true;
 }
@@ -224,7 +231,7 @@ __device__ void load_role(const CUtensorMap* tm_q, const CUtensorMap* tm_k, cons
   Item it;
   for (int k = 0; ok && item_at<SP>(p, k, it); ++k) {
     for (int t = 0; t < 2 && ok; ++t) {
-      if (it.n(t) == 0) continue;
+      if (it.kept(t) == 0) continue;
       if (q_cnt[t] > 0) {
         ok = bounded_wait(&sm.q_empty[t], (q_cnt[t] - 1) & 1, sm.abort_flag, p.err, kSiteQEmpty);
         if (!ok) break;
@@ -388,6 +395,99 @@ __device__ void mma_role(const Smem& sm, uint32_t tmem, const FwdParams& p) {
 #endif
 }
 
+// Block-sparse issuer. The two Q tiles walk the union of their masks' K/V tiles
+// (one copy of each), but tile t's products run only on the steps its mask
+// keeps. Per union step j: O_t += P_t V_j where tile t keeps j, then S_t(j+1)
+// where it keeps j+1 (after the tile's last P V, which read the TMEM columns
+// S_t overwrites). A tile's next S may lie many steps ahead, so V_j is released
+// by a commit after the P V of its last reader rather than by that reader's
+// next S, and a tile's O is complete after its last kept step.
+template <int D>
+__device__ void mma_role_sparse(const Smem& sm, uint32_t tmem, const FwdParams& p) {
+  using C = Cfg<D, false>;
+  const uint32_t ring_base = smem_u32(sm.ring);
+  const uint32_t qa0 = smem_u32(sm.q[0]);
+  const uint32_t qa1 = smem_u32(sm.q[1]);
+  auto slot_addr = [&](uint32_t r) { return ring_base + (r % C::kStages) * static_cast<uint32_t>(C::kTileBytes); };
+  auto wait_kv = [&](uint32_t r) {
+    return bounded_wait(&sm.kv_full[r % C::kStages], (r / C::kStages) & 1, sm.abort_flag, p.err, kSiteKvFull);
+  };
+  auto keeps = [](uint32_t word, int t) { return ((word >> (16 + t)) & 1u) != 0; };
+  uint32_t ring = 0;
+  uint32_t q_cnt[2] = {0, 0};
+  uint32_t p_cnt[2] = {0, 0};
+  uint32_t o_cnt[2] = {0, 0};
+  bool ok = true;
+  Item it;
+  for (int k = 0; ok && item_at<true>(p, k, it); ++k) {
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+      if (!ok || it.kept(t) == 0) continue;
+      ok = bounded_wait(&sm.q_full[t], q_cnt[t] & 1, sm.abort_flag, p.err, kSiteQFull);
+      ++q_cnt[t];
+    }
+    if (!ok) break;
+    const uint32_t base = ring;
+    const int nu = it.n_max();
+    ring = base + 2 * nu;
+    if (nu == 0) continue;
+    ok = wait_kv(base);
+    if (!ok) break;
+    uint32_t w = step_word<true>(it, 0);
+    tc_fence_after();
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+      if (!keeps(w, t)) continue;
+      qk_product<D, false>(tmem + C::s_col(t), t ? qa1 : qa0, slot_addr(base));
+      umma_commit(&sm.s_full[t]);
+    }
+    int done[2] = {0, 0};  // kept steps whose P V was issued, per tile
+    for (int j = 0; j < nu && ok; ++j) {
+      const uint32_t iv = base + 2 * j + 1;  // V_j
+      const uint32_t ik = base + 2 * j + 2;  // K_(j+1)
+      const uint32_t wn = (j + 1 < nu) ? step_word<true>(it, j + 1) : 0u;
+      ok = wait_kv(iv);  // V_j, and K_(j+1) if the union has it (both land on V_j's barrier)
+      if (!ok) break;
+      const int last_v = keeps(w, 1) ? 1 : 0;
+#pragma unroll
+      for (int t = 0; t < 2; ++t) {
+        if (!ok) continue;
+        if (keeps(w, t)) {
+          ok = bounded_wait(&sm.p_full[t], p_cnt[t] & 1, sm.abort_flag, p.err, kSitePFull);
+          ++p_cnt[t];
+          if (ok && done[t] == 0 && o_cnt[t] > 0)
+            ok = bounded_wait(&sm.o_empty[t], (o_cnt[t] - 1) & 1, sm.abort_flag, p.err, kSiteOEmpty);
+          if (!ok) continue;
+          tc_fence_after();
+          pv_product<D, false>(tmem + C::o_col(t), tmem + C::s_col(t), slot_addr(iv), done[t] > 0);
+          ++done[t];
+          if (t == last_v) umma_commit(&sm.kv_empty[iv % C::kStages]);
+          if (done[t] == it.kept(t)) {
+            umma_commit(&sm.o_full[t]);
+            ++o_cnt[t];
+          }
+        }
+        if (keeps(wn, t)) {
+          qk_product<D, false>(tmem + C::s_col(t), t ? qa1 : qa0, slot_addr(ik));
+          umma_commit(&sm.s_full[t]);
+        }
+      }
+      w = wn;
+    }
+  }
+  // Teardown: every product issued so far must finish before TMEM is freed.
+  umma_commit(sm.mma_done);
+  bounded_wait(sm.mma_done, 0, nullptr, p.err, kSiteDrain);
+#ifdef FA_DEBUG
+  sm.dbg[3] = ring;
+  for (int t = 0; t < 2; ++t) {
+    sm.dbg[4 + t] = q_cnt[t];
+    sm.dbg[6 + t] = p_cnt[t];
+    sm.dbg[8 + t] = o_cnt[t];
+  }
+#endif
+}
+
 // The tile whose products read K_j and V_j last (tile 1 unless it stops earlier).
 __device__ __forceinline__ int last_reader(const Item& it, int j) { return (it.n1 > j) ? 1 : 0; }
 
@@ -429,27 +529,49 @@ __device__ void softmax_role(const Smem& sm, uint32_t tmem, const FwdParams& p, 
     const uint32_t ring_base = ring_next;  // K_j is ring_base + 2j, V_j is ring_base + 2j + 1
     ring_next += 2 * it.n_max();
     const int nkv = it.n(t);
-    if (nkv == 0) continue;
     const int q_row = it.row(t) + row;
+    if (SP && it.kept(t) == 0) {
+      // the mask keeps no K/V tile for these rows: o = 0, lse = -inf
+      if (q_row < p.N) {
+        uint4* dst4 = reinterpret_cast<uint4*>(p.o + (static_cast<size_t>(it.bh) * p.N + q_row) * D);
+#pragma unroll
+        for (int i = 0; i < D / 8; ++i) dst4[i] = make_uint4(0u, 0u, 0u, 0u);
+        p.lse[static_cast<size_t>(it.bh) * p.N + q_row] = -INFINITY;
+      }
+      continue;
+    }
+    if (nkv == 0) continue;
     const int vis_end = p.causal ? min(q_row + 1, p.N) : p.N;  // keys [0, vis_end) are visible to this row
     float m_used = -INFINITY;  // base of every exponent so far (log2 domain, scaled)
     float l = 0.f;
     uint32_t next_word = SP ? step_word<SP>(it, 0) : 0u;
+    int kept_done = 0;  // block-sparse: kept steps of this tile so far
     for (int j = 0; j < nkv; ++j) {
       // K/V tile of step j, and whether this Q tile keeps it
       int jt = j;
-      bool keep = true;
+      bool last_k = false;  // block-sparse: this tile reads K_j last
       if constexpr (SP) {
         const uint32_t word = next_word;
         if (j + 1 < nkv) next_word = step_word<SP>(it, j + 1);  // one step ahead
         jt = static_cast<int>(word & 0xffffu);
-        keep = ((word >> (16 + t)) & 1u) != 0;
+        if (((word >> (16 + t)) & 1u) == 0) continue;  // a step only the other tile computes
+        last_k = t == 1 || ((word >> 17) & 1u) == 0;
       }
       ok = bounded_wait(&sm.s_full[t], s_cnt & 1, sm.abort_flag, p.err, kSiteSFull);
       ++s_cnt;
       ok = __all_sync(kFull, ok);
       if (!ok) break;
-      if (releaser) release_after_s<D, F8>(sm, it, t, j, ring_base);
+      if (releaser) {
+        if constexpr (SP) {
+          // K_j once its last reader's S is done; V_j is released by the issuing
+          // thread's commit after its last P V; Q_t after the tile's last S
+          if (last_k) mbar_arrive(&sm.kv_empty[(ring_base + 2 * j) % C::kStages]);
+          if (kept_done + 1 == it.kept(t)) mbar_arrive(&sm.q_empty[t]);
+        } else {
+          release_after_s<D, F8>(sm, it, t, j, ring_base);
+        }
+      }
+      ++kept_done;
       tc_fence_after();
       if constexpr (F8) {
         // block-wise scales of the e4m3 inputs: Q tile and K tile j of this head
@@ -458,8 +580,8 @@ __device__ void softmax_role(const Smem& sm, uint32_t tmem, const FwdParams& p, 
         sl2x2 = f2_pack(sl2, sl2);
       }
 
-      // visible keys of this tile for this row (none when the block mask removes it)
-      const int lim = keep ? vis_end - jt * kBN : 0;
+      // visible keys of this tile for this row
+      const int lim = vis_end - jt * kBN;
       if constexpr (F8) {
         // e4m3 inputs: one pass over the row. The 128 raw scores are loaded once, their
         // maximum taken (scale > 0, so it commutes with the scaling), then
@@ -621,7 +743,8 @@ __device__ void softmax_role(const Smem& sm, uint32_t tmem, const FwdParams& p, 
     ok = __all_sync(kFull, ok);
     if (!ok) break;
     // the last P V of this tile is done: its V tile is free if this tile was its last reader
-    if (releaser && last_reader(it, nkv - 1) == t)
+    // (block-sparse: every V is released by the issuing thread)
+    if (!SP && releaser && last_reader(it, nkv - 1) == t)
       mbar_arrive(&sm.kv_empty[(ring_base + 2 * (nkv - 1) + 1) % C::kStages]);
     tc_fence_after();
 
@@ -669,7 +792,8 @@ __device__ void softmax_role(const Smem& sm, uint32_t tmem, const FwdParams& p, 
 
 // Block-sparse step lists: one warp per (mask head, Q-tile pair) compacts, in
 // increasing order, the K/V tiles kept by either Q tile of the pair (the block
-// mask and, under the causal mask, j <= the Q tile's index).
+// mask and, under the causal mask, j <= the Q tile's index), and counts the
+// union's steps and the steps each Q tile keeps.
 __global__ void __launch_bounds__(32) sparse_list_kernel(const uint8_t* __restrict__ mask, int tiles, int pairs,
                                                          int causal, uint32_t* __restrict__ list,
                                                          int* __restrict__ cnt) {
@@ -677,7 +801,7 @@ __global__ void __launch_bounds__(32) sparse_list_kernel(const uint8_t* __restri
   const uint8_t* mk = mask + static_cast<size_t>(mh) * tiles * tiles;
   const int i0 = 2 * pair, i1 = 2 * pair + 1;
   uint32_t* out = list + (static_cast<size_t>(mh) * pairs + pair) * tiles;
-  int n = 0;
+  int n = 0, n0 = 0, n1 = 0;
   for (int base = 0; base < tiles; base += 32) {
     const int j = base + lane;
     bool a0 = false, a1 = false;
@@ -690,13 +814,14 @@ __global__ void __launch_bounds__(32) sparse_list_kernel(const uint8_t* __restri
       out[n + __popc(keep & ((1u << lane) - 1u))] =
           static_cast<uint32_t>(j) | (a0 ? 1u << 16 : 0u) | (a1 ? 1u << 17 : 0u);
     n += __popc(keep);
+    n0 += __popc(__ballot_sync(0xffffffffu, a0));
+    n1 += __popc(__ballot_sync(0xffffffffu, a1));
   }
   if (lane == 0) {
-    if (n == 0) {
-      out[0] = 0;  // tile 0, kept by neither: the rows get o = 0, lse = -inf
-      n = 1;
-    }
-    cnt[static_cast<size_t>(mh) * pairs + pair] = n;
+    int* c = cnt + 3 * (static_cast<size_t>(mh) * pairs + pair);
+    c[0] = n;
+    c[1] = n0;
+    c[2] = n1;
   }
 }
 
@@ -740,7 +865,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kLoadWarp) {
     if (lane == 0) load_role<D, F8, SP>(&tm_q, &tm_k, &tm_v, sm, p);
   } else if (warp == kMmaWarp) {
-    if (lane == 0) mma_role<D, F8, SP>(sm, tmem, p);
+    if (lane == 0) {
+      if constexpr (SP)
+        mma_role_sparse<D>(sm, tmem, p);
+      else
+        mma_role<D, F8, SP>(sm, tmem, p);
+    }
   } else {
     softmax_role<D, F8, SP>(sm, tmem, p, warp, lane);
   }

@@ -114,8 +114,9 @@ fa_status fa_fwd_host(const void *q, const void *k, const void *v, void *o, floa
  *            mask[i / 128][j / 128] != 0 and, if causal, j <= i.
  *   mask_heads  1 (one mask for every head) or H (head h uses mask h).
  * A row with no visible key gets o = 0 and lse = -inf.
- * Workspace: mask_heads*ceil(N/256)*(T+1)*4 bytes of stream-ordered device
- *   memory (the per Q-tile-pair step lists a first small kernel builds).
+ * Workspace: mask_heads*ceil(N/256)*(T+3)*4 bytes of stream-ordered device
+ *   memory (the per Q-tile-pair step lists and counts a first small kernel
+ *   builds).
  * Errors: as fa_fwd; FA_ERR_INVALID_ARG also for a NULL mask or another
  *   mask_heads.
  */
@@ -125,8 +126,9 @@ fa_status fa_fwd_sparse(const void *q, const void *k, const void *v, const uint8
 /*
  * Work plan of fa_fwd_sparse (host only; mask is a HOST pointer, same layout):
  * pairs_allowed = (Q tile, K/V tile) block pairs the mask (and the causal
- * rule) keeps, over all B*H heads; pairs_computed = pairs the kernel computes
- * (each pair of Q tiles walks the union of their kept K/V tiles, at least one).
+ * rule) keeps, over all B*H heads; pairs_computed = pairs whose products the
+ * kernel runs: each Q tile computes exactly the pairs its mask keeps (the two
+ * Q tiles of a work item share the copies of the union of their K/V tiles).
  */
 fa_status fa_fwd_sparse_plan(const uint8_t *mask, int mask_heads, int B, int H, int N, int causal,
                              long long *pairs_allowed, long long *pairs_computed);

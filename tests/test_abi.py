@@ -301,8 +301,8 @@ def test_sparse_plan_matches_the_pages_counts(lib):
     assert fa.fa_fwd_sparse_plan(ones, 2, 3, N) == (2 * 3 * T * T, 2 * 3 * T * T)
     allowed, computed = fa.fa_fwd_sparse_plan(ones, 1, 1, N, causal=True)
     assert allowed == T * (T + 1) // 2 == 36
-    # each pair of Q tiles walks the union of its K/V tiles: (i0 + 2) steps for both tiles
-    assert computed == sum(2 * (i0 + 2) for i0 in range(0, T, 2))
+    # each Q tile computes exactly the pairs its mask (and the causal rule) keeps
+    assert computed == allowed
     quarter = np.zeros((T, T), np.uint8)
     quarter[:, ::4] = 1
     allowed, _ = fa.fa_fwd_sparse_plan(quarter, 1, 1, N)
