@@ -544,17 +544,17 @@ __device__ void softmax_role(const Smem& sm, uint32_t tmem, const FwdParams& p, 
     const int vis_end = p.causal ? min(q_row + 1, p.N) : p.N;  // keys [0, vis_end) are visible to this row
     float m_used = -INFINITY;  // base of every exponent so far (log2 domain, scaled)
     float l = 0.f;
-    uint32_t next_word = SP ? step_word<SP>(it, 0) : 0u;
-    int kept_done = 0;  // block-sparse: kept steps of this tile so far
-    for (int j = 0; j < nkv; ++j) {
-      // K/V tile of step j, and whether this Q tile keeps it
-      int jt = j;
-      bool last_k = false;  // block-sparse: this tile reads K_j last
+    // dense: steps j = 0 .. nkv-1; block-sparse: the kept(t) steps of the union
+    // this tile's mask keeps, u walking the union (K_u, V_u at ring_base + 2u)
+    const int steps = SP ? it.kept(t) : nkv;
+    int u = 0;
+    for (int j = 0; j < steps; ++j) {
+      int jt = j;  // K/V tile of this step
+      bool last_k = false;  // block-sparse: this tile reads K_u last
       if constexpr (SP) {
-        const uint32_t word = next_word;
-        if (j + 1 < nkv) next_word = step_word<SP>(it, j + 1);  // one step ahead
+        uint32_t word = step_word<SP>(it, u);
+        while (((word >> (16 + t)) & 1u) == 0) word = step_word<SP>(it, ++u);
         jt = static_cast<int>(word & 0xffffu);
-        if (((word >> (16 + t)) & 1u) == 0) continue;  // a step only the other tile computes
         last_k = t == 1 || ((word >> 17) & 1u) == 0;
       }
       ok = bounded_wait(&sm.s_full[t], s_cnt & 1, sm.abort_flag, p.err, kSiteSFull);
@@ -563,15 +563,15 @@ __device__ void softmax_role(const Smem& sm, uint32_t tmem, const FwdParams& p, 
       if (!ok) break;
       if (releaser) {
         if constexpr (SP) {
-          // K_j once its last reader's S is done; V_j is released by the issuing
+          // K_u once its last reader's S is done; V_u is released by the issuing
           // thread's commit after its last P V; Q_t after the tile's last S
-          if (last_k) mbar_arrive(&sm.kv_empty[(ring_base + 2 * j) % C::kStages]);
-          if (kept_done + 1 == it.kept(t)) mbar_arrive(&sm.q_empty[t]);
+          if (last_k) mbar_arrive(&sm.kv_empty[(ring_base + 2 * u) % C::kStages]);
+          if (j + 1 == steps) mbar_arrive(&sm.q_empty[t]);
         } else {
           release_after_s<D, F8>(sm, it, t, j, ring_base);
         }
       }
-      ++kept_done;
+      if constexpr (SP) ++u;
       tc_fence_after();
       if constexpr (F8) {
         // block-wise scales of the e4m3 inputs: Q tile and K tile j of this head
