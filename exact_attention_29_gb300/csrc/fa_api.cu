@@ -367,8 +367,9 @@ fa_status fa_fwd_sparse(const void* q, const void* k, const void* v, const uint8
   FA_REJECT_IF(causal != 0 && causal != 1, FA_ERR_INVALID_ARG);
   FA_REJECT_IF(d != 64 && d != 128, FA_ERR_UNSUPPORTED);
   const long long bh = static_cast<long long>(B) * H;
-  const long long pairs = (static_cast<long long>(N) + 255) / 256;
-  FA_REJECT_IF(bh > 0x7fffffffLL || pairs > 65535, FA_ERR_INVALID_ARG);
+  // the step lists hold a K/V tile index + 1 in 16 bits
+  const long long tiles_ll = (static_cast<long long>(N) + 127) / 128;
+  FA_REJECT_IF(bh > 0x7fffffffLL || tiles_ll > 65535, FA_ERR_INVALID_ARG);
   int dev = -1;
   fa_status st = current_device(&dev);
   if (st != FA_OK) return st;
@@ -378,7 +379,8 @@ fa_status fa_fwd_sparse(const void* q, const void* k, const void* v, const uint8
   const size_t tiles = (static_cast<size_t>(N) + 127) / 128;
   const size_t rows = static_cast<size_t>(mask_heads) * ((static_cast<size_t>(N) + 255) / 256);
   void* ws = nullptr;
-  st = ws_alloc(dev, &ws, rows * tiles * sizeof(uint32_t) + 3 * rows * sizeof(int), s,
+  // step lists, their counts, and the forward's run-time item counter
+  st = ws_alloc(dev, &ws, rows * tiles * sizeof(uint32_t) + (3 * rows + 1) * sizeof(int), s,
                 "workspace allocation (block-sparse step lists)");
   if (st != FA_OK) return st;
   cudaError_t e = cudaSuccess;

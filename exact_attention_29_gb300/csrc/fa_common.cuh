@@ -30,6 +30,8 @@ enum WaitSite : int {
   kSiteDrain = 7,
   kSiteQEmpty = 8,
   kSiteOEmpty = 9,
+  kSiteItemFull = 10,   // block-sparse forward: the next item index was published
+  kSiteItemEmpty = 11,  // block-sparse forward: an item slot was read by every role
   kSiteCheckFwd = 20,  // FA_DEBUG: the forward's roles disagree (items, ring, phases)
   kSiteCheckBwd = 21,  // FA_DEBUG: the backward's roles completed different tile counts
   kSiteCheckGqa = 22,  // FA_DEBUG: the GQA decode's roles disagree on the tiles of a split

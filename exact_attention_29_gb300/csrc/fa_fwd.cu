@@ -64,6 +64,12 @@ constexpr int kLoadWarp = 9;
 constexpr float kRescaleSlack = 8.0f;  // log2 units: rescale only when the max grows by > 2^8
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr uint32_t kFull = 0xffffffffu;
+// Block-sparse items are handed out at run time: the loading thread takes the
+// next item index from a global counter and publishes it to the CTA's other
+// roles through this many shared-memory slots.
+constexpr int kItemSlots = 4;
+// arrivals that free an item slot: the MMA thread and one lane per softmax warp
+constexpr int kItemReaders = 1 + 8;
 
 // F8: e4m3 Q, K and V^T (d = 128 only: a 128-byte row is one swizzle chunk).
 template <int D, bool F8 = false>
@@ -78,10 +84,11 @@ struct Cfg {
   static constexpr uint32_t kTmemCols = 512;
   static constexpr int kRingOff = 2 * kTileBytes;
   static constexpr int kBarOff = kRingOff + kStages * kTileBytes;
-  // q_full, q_empty, s_full, p_full, o_full, o_empty (2 each), kv_full, kv_empty, mma_done
-  static constexpr int kNumBars = 12 + 2 * kStages + 1;
-  // + TMEM slot, abort flag, 16 protocol counters (FA_DEBUG), slack to align to 1 KB
-  static constexpr int kSmemBytes = kBarOff + kNumBars * 8 + 16 + 64 + 1024;
+  // q_full, q_empty, s_full, p_full, o_full, o_empty (2 each), kv_full, kv_empty, mma_done,
+  // item_full, item_empty
+  static constexpr int kNumBars = 12 + 2 * kStages + 1 + 2 * kItemSlots;
+  // + TMEM slot, abort flag, 16 protocol counters (FA_DEBUG), item slots, slack to align to 1 KB
+  static constexpr int kSmemBytes = kBarOff + kNumBars * 8 + 16 + 64 + 4 * kItemSlots + 1024;
 };
 
 struct FwdParams {
@@ -100,6 +107,7 @@ struct FwdParams {
   // number of those steps Q tile 0 and Q tile 1 keep
   const uint32_t* list;
   const int* cnt;
+  int* next_item;  // block-sparse: the run-time item counter (zeroed by sparse_list_kernel)
   int mask_heads;
   int H;
   int N;
@@ -124,9 +132,12 @@ struct Smem {
   uint64_t* kv_full;   // [S]   K or V tile landed in a ring slot
   uint64_t* kv_empty;  // [S]   ring slot free again (softmax arrives)
   uint64_t* mma_done;  // [1]   every product done (teardown)
+  uint64_t* item_full;   // [kItemSlots] block-sparse: an item index was published in the slot
+  uint64_t* item_empty;  // [kItemSlots] block-sparse: every role has read the slot (kItemReaders arrivals)
   uint32_t* tmem_slot;
   volatile int* abort_flag;
   uint32_t* dbg;       // [16] per-role protocol counters, compared at the end (FA_DEBUG builds)
+  volatile int* item_q;  // [kItemSlots] block-sparse: published item indices
 };
 
 template <int D, bool F8>
@@ -148,9 +159,12 @@ __device__ __forceinline__ Smem carve(uint8_t* raw) {
   s.kv_full = bars + 12;
   s.kv_empty = s.kv_full + C::kStages;
   s.mma_done = s.kv_empty + C::kStages;
-  s.tmem_slot = reinterpret_cast<uint32_t*>(s.mma_done + 1);
+  s.item_full = s.mma_done + 1;
+  s.item_empty = s.item_full + kItemSlots;
+  s.tmem_slot = reinterpret_cast<uint32_t*>(s.item_empty + kItemSlots);
   s.abort_flag = reinterpret_cast<volatile int*>(s.tmem_slot + 1);
   s.dbg = reinterpret_cast<uint32_t*>(s.tmem_slot + 4);
+  s.item_q = reinterpret_cast<volatile int*>(s.dbg + 16);
   return s;
 }
 
@@ -181,12 +195,9 @@ __device__ __forceinline__ uint32_t step_word(const Item& it, int j) {
   return __ldg(it.list + j);
 }
 
-// k-th item of this CTA (snake order over the heavy-first item list), or false.
+// Item w of the heavy-first item list, or false past its end.
 template <bool SP>
-__device__ __forceinline__ bool item_at(const FwdParams& p, int k, Item& it) {
-  const int G = static_cast<int>(gridDim.x);
-  const int c = static_cast<int>(blockIdx.x);
-  const long long w = static_cast<long long>(k) * G + ((k & 1) ? (G - 1 - c) : c);
+__device__ __forceinline__ bool item_decode(const FwdParams& p, long long w, Item& it) {
   if (w >= p.num_items) return false;
   const int rank = static_cast<int>(w / p.BH);
   it.bh = static_cast<int>(w - static_cast<long long>(rank) * p.BH);
@@ -217,6 +228,56 @@ __device__ __forceinline__ bool item_at(const FwdParams& p, int k, Item& it) {
   return true;
 }
 
+// Dense: the k-th item of this CTA, dealt in a snake order over the
+// heavy-first list (the causal load balances by construction).
+__device__ __forceinline__ bool item_at(const FwdParams& p, int k, Item& it) {
+  const int G = static_cast<int>(gridDim.x);
+  const int c = static_cast<int>(blockIdx.x);
+  return item_decode<false>(p, static_cast<long long>(k) * G + ((k & 1) ? (G - 1 - c) : c), it);
+}
+
+// Block-sparse items differ in cost by the number of K/V tiles their masks
+// keep (a global row keeps them all), so a static deal leaves some CTAs with
+// far more work; they are handed out at run time instead, in list order
+// (greedy list scheduling). The loading thread publishes item k of this CTA
+// in slot k % kItemSlots; the other roles read it from there (fetch_item).
+__device__ __forceinline__ bool publish_item(const Smem& sm, const FwdParams& p, int k, int idx, bool& ok) {
+  const int e = k % kItemSlots;
+  const uint32_t use = static_cast<uint32_t>(k / kItemSlots);
+  if (use > 0) {
+    ok = bounded_wait(&sm.item_empty[e], (use - 1) & 1, sm.abort_flag, p.err, kSiteItemEmpty);
+    if (!ok) return false;
+  }
+  sm.item_q[e] = idx;
+  mbar_arrive(&sm.item_full[e]);  // releases the store above to the slot's readers
+  return true;
+}
+
+// Item k of this CTA as published by the loading thread. `warp_reader`: the
+// caller is a full warp (one arrival from lane 0 after every lane has read
+// the slot); otherwise a single thread (the MMA issuer).
+template <bool SP>
+__device__ __forceinline__ bool fetch_item(const Smem& sm, const FwdParams& p, int k, Item& it, bool& ok,
+                                           bool warp_reader) {
+  if constexpr (!SP) {
+    return item_at(p, k, it);
+  } else {
+    const int e = k % kItemSlots;
+    ok = bounded_wait(&sm.item_full[e], static_cast<uint32_t>(k / kItemSlots) & 1, sm.abort_flag, p.err,
+                      kSiteItemFull);
+    if (warp_reader) ok = __all_sync(kFull, ok);
+    if (!ok) return false;
+    const int idx = sm.item_q[e];
+    if (warp_reader) {
+      __syncwarp();
+      if ((threadIdx.x & 31) == 0) mbar_arrive(&sm.item_empty[e]);
+    } else {
+      mbar_arrive(&sm.item_empty[e]);
+    }
+    return item_decode<true>(p, idx, it);
+  }
+}
+
 // ---------------------------------------------------------------- TMA producer (one thread)
 template <int D, bool F8, bool SP>
 __device__ void load_role(const CUtensorMap* tm_q, const CUtensorMap* tm_k, const CUtensorMap* tm_v, const Smem& sm,
@@ -229,7 +290,18 @@ __device__ void load_role(const CUtensorMap* tm_q, const CUtensorMap* tm_k, cons
   uint32_t q_cnt[2] = {0, 0};   // Q tiles issued per buffer
   bool ok = true;
   Item it;
-  for (int k = 0; ok && item_at<SP>(p, k, it); ++k) {
+  // block-sparse: the next item index is taken one item ahead, so the atomic's
+  // latency overlaps this item's copies
+  int idx_next = SP ? atomicAdd(p.next_item, 1) : 0;
+  for (int k = 0; ok; ++k) {
+    if constexpr (SP) {
+      const int idx = idx_next;
+      if (!publish_item(sm, p, k, idx, ok)) break;
+      if (!item_decode<true>(p, idx, it)) break;
+      idx_next = atomicAdd(p.next_item, 1);
+    } else {
+      if (!item_at(p, k, it)) break;
+    }
     for (int t = 0; t < 2 && ok; ++t) {
       if (it.kept(t) == 0) continue;
       if (q_cnt[t] > 0) {
@@ -332,7 +404,7 @@ __device__ void mma_role(const Smem& sm, uint32_t tmem, const FwdParams& p) {
   uint32_t o_cnt[2] = {0, 0};        // items whose O_t was produced
   bool ok = true;
   Item it;
-  for (int k = 0; ok && item_at<SP>(p, k, it); ++k) {
+  for (int k = 0; ok && fetch_item<SP>(sm, p, k, it, ok, false); ++k) {
     for (int t = 0; t < 2 && ok; ++t) {
       if (it.n(t) == 0) continue;
       ok = bounded_wait(&sm.q_full[t], q_cnt[t] & 1, sm.abort_flag, p.err, kSiteQFull);
@@ -419,7 +491,7 @@ __device__ void mma_role_sparse(const Smem& sm, uint32_t tmem, const FwdParams& 
   uint32_t o_cnt[2] = {0, 0};
   bool ok = true;
   Item it;
-  for (int k = 0; ok && item_at<true>(p, k, it); ++k) {
+  for (int k = 0; ok && fetch_item<true>(sm, p, k, it, ok, false); ++k) {
 #pragma unroll
     for (int t = 0; t < 2; ++t) {
       if (!ok || it.kept(t) == 0) continue;
@@ -525,7 +597,7 @@ __device__ void softmax_role(const Smem& sm, uint32_t tmem, const FwdParams& p, 
   Item it;
   const bool releaser = (quarter == 0 && lane == 0);  // one thread per tile releases buffers
   uint32_t ring_next = 0;                             // K/V ring position of the next item
-  for (int k = 0; ok && item_at<SP>(p, k, it); ++k) {
+  for (int k = 0; ok && fetch_item<SP>(sm, p, k, it, ok, true); ++k) {
     const uint32_t ring_base = ring_next;  // K_j is ring_base + 2j, V_j is ring_base + 2j + 1
     ring_next += 2 * it.n_max();
     const int nkv = it.n(t);
@@ -796,8 +868,9 @@ __device__ void softmax_role(const Smem& sm, uint32_t tmem, const FwdParams& p, 
 // union's steps and the steps each Q tile keeps.
 __global__ void __launch_bounds__(32) sparse_list_kernel(const uint8_t* __restrict__ mask, int tiles, int pairs,
                                                          int causal, uint32_t* __restrict__ list,
-                                                         int* __restrict__ cnt) {
+                                                         int* __restrict__ cnt, int* __restrict__ next_item) {
   const int pair = blockIdx.x, mh = blockIdx.y, lane = threadIdx.x;
+  if (pair == 0 && mh == 0 && lane == 0) *next_item = 0;  // the forward's run-time item counter
   const uint8_t* mk = mask + static_cast<size_t>(mh) * tiles * tiles;
   const int i0 = 2 * pair, i1 = 2 * pair + 1;
   uint32_t* out = list + (static_cast<size_t>(mh) * pairs + pair) * tiles;
@@ -849,6 +922,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&sm.kv_empty[s], 1);
     }
     mbar_init(sm.mma_done, 1);
+    for (int e = 0; e < kItemSlots; ++e) {
+      mbar_init(&sm.item_full[e], 1);
+      mbar_init(&sm.item_empty[e], kItemReaders);
+    }
     *sm.abort_flag = 0;
     for (int i = 0; i < 16; ++i) sm.dbg[i] = 0;
     fence_barrier_init();
@@ -935,7 +1012,8 @@ fa_status launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap
 template <int D>
 fa_status launch_bf16(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
                       int causal, float scale, cudaStream_t stream, unsigned int* err, int num_sms,
-                      const uint32_t* list = nullptr, const int* cnt = nullptr, int mask_heads = 0) {
+                      const uint32_t* list = nullptr, const int* cnt = nullptr, int mask_heads = 0,
+                      int* next_item = nullptr) {
   CUtensorMap tq, tk, tv;
   const uint64_t bh = static_cast<uint64_t>(B) * H;
   if (!encode_bf16_map(&tq, q, D, N, bh, kBM) || !encode_bf16_map(&tk, k, D, N, bh, kBN) ||
@@ -947,6 +1025,7 @@ fa_status launch_bf16(const void* q, const void* k, const void* v, void* o, floa
   prm.err = err;
   prm.list = list;
   prm.cnt = cnt;
+  prm.next_item = next_item;
   prm.mask_heads = mask_heads;
   if (list != nullptr) return launch<D, false, true>(tq, tk, tv, prm, B, H, N, causal, scale, stream, num_sms);
   return launch<D, false, false>(tq, tk, tv, prm, B, H, N, causal, scale, stream, num_sms);
@@ -967,16 +1046,19 @@ fa_status launch_fwd_sparse(const void* q, const void* k, const void* v, const u
   if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
   const int tiles = (N + kBM - 1) / kBM;
   const int pairs = (N + 2 * kBM - 1) / (2 * kBM);
+  int* next_item = cnt_ws + 3 * static_cast<size_t>(pairs) * mask_heads;
   sparse_list_kernel<<<dim3(static_cast<unsigned>(pairs), static_cast<unsigned>(mask_heads)), 32, 0, stream>>>(
-      mask, tiles, pairs, causal ? 1 : 0, list_ws, cnt_ws);
+      mask, tiles, pairs, causal ? 1 : 0, list_ws, cnt_ws, next_item);
   const cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) {
     set_error_text("sparse_list_kernel launch", e);
     return FA_ERR_CUDA;
   }
   if (d == 128)
-    return launch_bf16<128>(q, k, v, o, lse, B, H, N, causal, scale, stream, err, num_sms, list_ws, cnt_ws, mask_heads);
-  return launch_bf16<64>(q, k, v, o, lse, B, H, N, causal, scale, stream, err, num_sms, list_ws, cnt_ws, mask_heads);
+    return launch_bf16<128>(q, k, v, o, lse, B, H, N, causal, scale, stream, err, num_sms, list_ws, cnt_ws, mask_heads,
+                            next_item);
+  return launch_bf16<64>(q, k, v, o, lse, B, H, N, causal, scale, stream, err, num_sms, list_ws, cnt_ws, mask_heads,
+                         next_item);
 }
 
 fa_status launch_fwd_fp8(const void* q8, const void* k8, const void* vt8, const float* q_scale, const float* k_scale,

@@ -52,7 +52,8 @@ fa_status launch_quantize_fp8(const void* x, const float* signs, void* codes, fl
                               int per_head, int transpose, int v_pitch, float* amax_ws, cudaStream_t stream);
 
 // Block-sparse forward: mask [mask_heads][T][T] bytes on the device, T = ceil(N / 128);
-// list_ws: uint32 [mask_heads][ceil(N/256)][T] and cnt_ws: int [mask_heads][ceil(N/256)][3] scratch.
+// list_ws: uint32 [mask_heads][ceil(N/256)][T] and cnt_ws: int [mask_heads][ceil(N/256)][3] + 1 scratch
+// (the last int is the forward's run-time item counter).
 fa_status launch_fwd_sparse(const void* q, const void* k, const void* v, const uint8_t* mask, int mask_heads, void* o,
                             float* lse, int B, int H, int N, int d, int causal, float scale, uint32_t* list_ws,
                             int* cnt_ws, cudaStream_t stream, unsigned int* err, int num_sms);

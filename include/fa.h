@@ -114,11 +114,11 @@ fa_status fa_fwd_host(const void *q, const void *k, const void *v, void *o, floa
  *            mask[i / 128][j / 128] != 0 and, if causal, j <= i.
  *   mask_heads  1 (one mask for every head) or H (head h uses mask h).
  * A row with no visible key gets o = 0 and lse = -inf.
- * Workspace: mask_heads*ceil(N/256)*(T+3)*4 bytes of stream-ordered device
- *   memory (the per Q-tile-pair step lists and counts a first small kernel
- *   builds).
- * Errors: as fa_fwd; FA_ERR_INVALID_ARG also for a NULL mask or another
- *   mask_heads.
+ * Workspace: mask_heads*ceil(N/256)*(T+3)*4 + 4 bytes of stream-ordered
+ *   device memory (the per Q-tile-pair step lists and counts a first small
+ *   kernel builds, and the counter that hands out work items at run time).
+ * Errors: as fa_fwd; FA_ERR_INVALID_ARG also for a NULL mask, another
+ *   mask_heads, or T > 65535 (N > 8,388,480).
  */
 fa_status fa_fwd_sparse(const void *q, const void *k, const void *v, const uint8_t *mask, int mask_heads, void *o,
                         float *lse, int B, int H, int N, int d, int causal, float scale, fa_stream_t stream);
@@ -316,7 +316,8 @@ fa_status fa_check_device_error(fa_stream_t stream);
  * Site code of the first wait or check that failed, as read by the most recent
  * fa_check_device_error on the calling thread (0 if that call found none).
  * Codes: 1 Q landed, 2 K/V landed, 3 K/V slot free, 4 S done, 5 P written,
- * 6 O done, 7 teardown drain, 8 Q buffer free, 9 O read out, 20-22 FA_DEBUG
+ * 6 O done, 7 teardown drain, 8 Q buffer free, 9 O read out, 10 block-sparse
+ * work item published, 11 block-sparse work item slot free, 20-22 FA_DEBUG
  * protocol checks (forward, backward, GQA decode), 100 the timeout self-test.
  */
 int fa_last_error_site(void);

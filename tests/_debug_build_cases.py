@@ -33,6 +33,14 @@ def main(out_path):
         T = (N + 127) // 128
         mask = (torch.rand((3, T, T), generator=torch.Generator().manual_seed(N)) < 0.5).to(torch.uint8).cuda()
         keep(f"sparse_{N}_{d}_{int(causal)}", *fa.fa_fwd_sparse(q, k, v, mask, causal=causal))
+    # block-sparse over 32 tiles: band + global + random rows, some block rows
+    # keeping everything and some nothing (uneven private runs within a pair)
+    for d, causal in ((128, False), (64, True)):
+        q, k, v = wl.prefill_inputs(1, 3, 4000, d, seed=d, device="cuda")
+        mask = wl.block_mask_bigbird(32, heads=3, seed=d)
+        mask[:, 5::7, :] = 1
+        mask[:, 9::11, :] = 0
+        keep(f"sparse_mixed_{d}_{int(causal)}", *fa.fa_fwd_sparse(q, k, v, mask.cuda(), causal=causal))
     for N, causal in ((1000, True), (777, False)):
         q, k, v = wl.prefill_inputs(1, 2, N, 128, seed=N, device="cuda")
         signs = (torch.randint(0, 2, (128,), generator=torch.Generator().manual_seed(N)) * 2 - 1).float().cuda()

@@ -312,10 +312,13 @@ def test_sparse_plan_matches_the_pages_counts(lib):
 def test_sparse_rejects_bad_arguments(lib):
     import exact_attention_29_gb300 as fa
 
-    def sp(mask=16, mask_heads=1, H=2, d=128, scale=0.1):
-        return lib.fa_fwd_sparse(16, 16, 16, mask, mask_heads, 16, 16, 1, H, 300, d, 0, scale, None)
+    def sp(mask=16, mask_heads=1, H=2, d=128, scale=0.1, N=300):
+        return lib.fa_fwd_sparse(16, 16, 16, mask, mask_heads, 16, 16, 1, H, N, d, 0, scale, None)
 
     assert sp(mask=None) == fa.FA_ERR_INVALID_ARG
+    # step lists hold a K/V tile index + 1 in 16 bits: at most 65535 tiles of 128 keys
+    assert sp(N=65535 * 128 + 1) == fa.FA_ERR_INVALID_ARG
+    assert b"tiles_ll > 65535" in lib.fa_last_error_string()
     assert sp(mask_heads=3) == fa.FA_ERR_INVALID_ARG
     assert sp(scale=-1.0) == fa.FA_ERR_INVALID_ARG
     assert sp(d=96) == fa.FA_ERR_UNSUPPORTED

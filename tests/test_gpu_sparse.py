@@ -92,3 +92,42 @@ def test_bigbird_llama_shape_sampled_heads():
         sl = (slice(b, b + 1), slice(h, h + 1))
         o_ref, lse_ref = oracle.attention_block_mask(q[sl].cpu(), k[sl].cpu(), v[sl].cpu(), mask[h], c.causal, c.scale)
         _compare_sparse(o[sl], lse[sl], o_ref, lse_ref, f"bigbird head ({b},{h})")
+
+
+def _mixed_mask(H, T, seed):
+    """Per block row a different kind: dense, empty, one block, a random
+    density, a band; so the two Q tiles of a pair often keep very different
+    numbers of K/V tiles, share few of them, or one keeps none."""
+    g = torch.Generator().manual_seed(seed)
+    m = torch.zeros((H, T, T), dtype=torch.uint8)
+    for h in range(H):
+        for i in range(T):
+            kind = int(torch.randint(0, 5, (1,), generator=g))
+            if kind == 0:
+                m[h, i, :] = 1
+            elif kind == 2:
+                m[h, i, int(torch.randint(0, T, (1,), generator=g))] = 1
+            elif kind == 3:
+                dens = float(torch.rand((1,), generator=g))
+                m[h, i] = (torch.rand((T,), generator=g) < dens).to(torch.uint8)
+            elif kind == 4:
+                m[h, i, max(0, i - 2): i + 3] = 1
+    return m
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("d", [64, 128])
+def test_mixed_row_masks_many_tiles(d, causal):
+    """B1 H4 N4000 (32 tiles, a ragged last one): long private runs on one tile
+    of a pair and short ones on the other, rows that keep nothing next to rows
+    that keep everything; every head against the oracle."""
+    import exact_attention_29_gb300 as fa
+
+    B, H, N = 1, 4, 4000
+    T = (N + 127) // 128
+    q, k, v = wl.prefill_inputs(B, H, N, d, seed=17 + d)
+    mask = _mixed_mask(H, T, seed=d + int(causal))
+    o, lse = fa.fa_fwd_sparse(q.cuda(), k.cuda(), v.cuda(), mask.cuda(), causal=causal)
+    fa.fa_check_device_error()
+    o_ref, lse_ref = oracle.attention_block_mask(q, k, v, mask, causal, d ** -0.5)
+    _compare_sparse(o, lse, o_ref, lse_ref, f"mixed rows d={d} causal={causal}")
