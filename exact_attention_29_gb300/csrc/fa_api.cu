@@ -267,7 +267,7 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
   FA_REJECT_IF(d != 64 && d != 128, FA_ERR_UNSUPPORTED);
   const long long bh = static_cast<long long>(B) * H;
   const long long pairs = (static_cast<long long>(N) + 255) / 256;
-  FA_REJECT_IF(bh > 0x7fffffffLL || pairs > 65535, FA_ERR_INVALID_ARG);
+  FA_REJECT_IF(bh > 0x7fffffffLL || pairs > 65535 || bh * pairs > 0x7fffffffLL, FA_ERR_INVALID_ARG);
   int dev = -1;
   fa_status st = current_device(&dev);
   if (st != FA_OK) return st;
@@ -303,7 +303,7 @@ fa_status fa_fwd_host(const void* q, const void* k, const void* v, void* o, floa
   FA_REJECT_IF(d != 64 && d != 128, FA_ERR_UNSUPPORTED);
   const long long bh = static_cast<long long>(B) * H;
   const long long pairs = (static_cast<long long>(N) + 255) / 256;
-  FA_REJECT_IF(bh > 0x7fffffffLL || pairs > 65535, FA_ERR_INVALID_ARG);
+  FA_REJECT_IF(bh > 0x7fffffffLL || pairs > 65535 || bh * pairs > 0x7fffffffLL, FA_ERR_INVALID_ARG);
   int dev = -1;
   fa_status st = current_device(&dev);
   if (st != FA_OK) return st;
@@ -369,7 +369,8 @@ fa_status fa_fwd_sparse(const void* q, const void* k, const void* v, const uint8
   const long long bh = static_cast<long long>(B) * H;
   // the step lists hold a K/V tile index + 1 in 16 bits
   const long long tiles_ll = (static_cast<long long>(N) + 127) / 128;
-  FA_REJECT_IF(bh > 0x7fffffffLL || tiles_ll > 65535, FA_ERR_INVALID_ARG);
+  FA_REJECT_IF(bh > 0x7fffffffLL || tiles_ll > 65535 || bh * ((tiles_ll + 1) / 2) > 0x7fffffffLL,
+               FA_ERR_INVALID_ARG);
   int dev = -1;
   fa_status st = current_device(&dev);
   if (st != FA_OK) return st;
@@ -460,7 +461,7 @@ fa_status fa_fwd_fp8(const void* q8, const void* k8, const void* vt8, const floa
   FA_REJECT_IF(d != 128, FA_ERR_UNSUPPORTED);
   const long long bh = static_cast<long long>(B) * H;
   const long long pairs = (static_cast<long long>(N) + 255) / 256;
-  FA_REJECT_IF(bh > 0x7fffffffLL || pairs > 65535, FA_ERR_INVALID_ARG);
+  FA_REJECT_IF(bh > 0x7fffffffLL || pairs > 65535 || bh * pairs > 0x7fffffffLL, FA_ERR_INVALID_ARG);
   int dev = -1;
   fa_status st = current_device(&dev);
   if (st != FA_OK) return st;

@@ -74,7 +74,8 @@ typedef enum {
  *   causal   0: every row sees all N keys; 1: row i sees keys 0..i.
  *   scale    > 0 and finite, usually 1/sqrt(d).
  * Errors: FA_ERR_INVALID_ARG for null/misaligned pointers, sizes < 1, a bad
- *   scale, or sizes whose element counts overflow; FA_ERR_UNSUPPORTED for d;
+ *   scale, or sizes whose counts overflow (B*H and B*H*ceil(N/256) work items
+ *   above 2^31 - 1, ceil(N/256) above 65535); FA_ERR_UNSUPPORTED for d;
  *   FA_ERR_CUDA if the launch fails.
  */
 fa_status fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H, int N, int d,

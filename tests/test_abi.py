@@ -71,6 +71,9 @@ def test_fwd_rejects_bad_arguments(lib):
     assert _fwd(lib, d=96) == fa.FA_ERR_UNSUPPORTED
     assert _fwd(lib, d=256) == fa.FA_ERR_UNSUPPORTED
     assert _fwd(lib, N=65536 * 256 + 1) == fa.FA_ERR_INVALID_ARG  # more Q-tile pairs than the grid allows
+    # work items (batch x heads x Q-tile pairs) are counted in 32 bits
+    assert _fwd(lib, B=32768, H=32768, N=512) == fa.FA_ERR_INVALID_ARG
+    assert b"bh * pairs" in lib.fa_last_error_string()
 
 
 def test_host_buffer_fwd_rejects_bad_arguments(lib):
@@ -319,6 +322,9 @@ def test_sparse_rejects_bad_arguments(lib):
     # step lists hold a K/V tile index + 1 in 16 bits: at most 65535 tiles of 128 keys
     assert sp(N=65535 * 128 + 1) == fa.FA_ERR_INVALID_ARG
     assert b"tiles_ll > 65535" in lib.fa_last_error_string()
+    # work items (batch x heads x Q-tile pairs) are counted in 32 bits
+    assert lib.fa_fwd_sparse(16, 16, 16, 16, 1, 16, 16, 32768, 32768, 512, 128, 0, 0.1, None) == fa.FA_ERR_INVALID_ARG
+    assert b"bh * ((tiles_ll + 1) / 2)" in lib.fa_last_error_string()
     assert sp(mask_heads=3) == fa.FA_ERR_INVALID_ARG
     assert sp(scale=-1.0) == fa.FA_ERR_INVALID_ARG
     assert sp(d=96) == fa.FA_ERR_UNSUPPORTED
