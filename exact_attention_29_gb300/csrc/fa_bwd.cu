@@ -503,11 +503,21 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const int q0 = (i_first + it) * 128;
         const int nq = min(128, p.N - q0);
         float* dst = p.dq_acc + (head_rows + q0) * D + dcol;
-        // 32 queries (TMEM columns c0 ..) of this dQ column: scaled reductions
-        auto add32 = [&](const uint32_t (&r)[32], int c0) {
+        // 32 queries (TMEM columns c0 ..) of this dQ column: scaled reductions.
+        // `paced`: a 20 ns pause after every second reduction. The reductions
+        // that follow the release of the TMEM columns overlap the P/dS warps'
+        // next dS phase, whose shared-memory stores of dS^T queue behind them
+        // in the load/store path; spread over about a third of a Q-tile period
+        // they leave it free (measured: +5 to +7 % on the Llama and 16k shapes;
+        // 20 ns or more per reduction, or a pause after each one, loses ~20 %:
+        // the read-out then holds up the next release).
+        auto add32 = [&](const uint32_t (&r)[32], int c0, bool paced) {
           if (c0 + 32 <= nq) {
 #pragma unroll
-            for (int e = 0; e < 32; ++e) red_add_f32(dst + static_cast<size_t>(c0 + e) * D, __uint_as_float(r[e]) * p.scale);
+            for (int e = 0; e < 32; ++e) {
+              red_add_f32(dst + static_cast<size_t>(c0 + e) * D, __uint_as_float(r[e]) * p.scale);
+              if (paced && (e & 1)) __nanosleep(20);
+            }
           } else {
 #pragma unroll
             for (int e = 0; e < 32; ++e)
@@ -521,14 +531,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         tmem_ld_x32(dq_tm, r0);
         tmem_ld_x32(dq_tm + 32, r1);
         tmem_ld_x32(dq_tm + 64, r2);
-        add32(r0, 0);
+        add32(r0, 0, false);
         tmem_ld_x32(dq_tm + 96, r0);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars[kBarDqEmpty]);
-        add32(r1, 32);
-        add32(r2, 64);
-        add32(r0, 96);
+        add32(r1, 32, true);
+        add32(r2, 64, true);
+        add32(r0, 96, true);
       }
 #ifdef FA_DEBUG
       if (warp == 0 && lane == 0) dbg[3] = static_cast<uint32_t>(it);
