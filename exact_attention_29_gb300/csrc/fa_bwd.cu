@@ -107,27 +107,44 @@ struct BwdParams {
   float scale_log2;
 };
 
-// D_i = sum_c dO_ic O_ic in fp32, one thread per row.
+// Before the main kernel, in one pass over the rows: D_i = sum_c dO_ic O_ic in
+// fp32, and the row's fp32 dQ accumulator set to zero. D / 8 lanes share a row
+// (16 bytes of O and of dO each), so a warp's loads and stores cover whole
+// consecutive rows; the row sum is finished with shuffles.
+constexpr int kPrepThreads = 256;
+
 template <int D>
-__global__ void __launch_bounds__(256) bwd_delta_kernel(const __nv_bfloat16* __restrict__ o,
-                                                         const __nv_bfloat16* __restrict__ dout,
-                                                         float* __restrict__ delta, long long rows) {
-  const long long row = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (row >= rows) return;
-  const uint4* po = reinterpret_cast<const uint4*>(o + row * D);
-  const uint4* pd = reinterpret_cast<const uint4*>(dout + row * D);
-  float acc = 0.f;
-#pragma unroll 4
-  for (int i = 0; i < D / 8; ++i) {
-    const uint4 a = po[i], b = pd[i];
-    const uint32_t wa[4] = {a.x, a.y, a.z, a.w}, wb[4] = {b.x, b.y, b.z, b.w};
+__global__ void __launch_bounds__(kPrepThreads) bwd_prep_kernel(const __nv_bfloat16* __restrict__ o,
+                                                                const __nv_bfloat16* __restrict__ dout,
+                                                                float* __restrict__ delta, float* __restrict__ dq_acc,
+                                                                long long rows) {
+  constexpr int kLanesPerRow = D / 8;
+  constexpr int kRowsPerWarp = 32 / kLanesPerRow;
+  const int lane = static_cast<int>(threadIdx.x & 31);
+  const long long warp = (static_cast<long long>(blockIdx.x) * kPrepThreads + threadIdx.x) >> 5;
+  const long long warps = (static_cast<long long>(gridDim.x) * kPrepThreads) >> 5;
+  for (long long r0 = warp * kRowsPerWarp; r0 < rows; r0 += warps * kRowsPerWarp) {
+    const long long row = r0 + lane / kLanesPerRow;
+    const int c = lane % kLanesPerRow;
+    float acc = 0.f;
+    if (row < rows) {
+      const uint4 a = reinterpret_cast<const uint4*>(o + row * D)[c];
+      const uint4 b = reinterpret_cast<const uint4*>(dout + row * D)[c];
+      const uint32_t wa[4] = {a.x, a.y, a.z, a.w}, wb[4] = {b.x, b.y, b.z, b.w};
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      acc = fmaf(__uint_as_float(wa[e] << 16), __uint_as_float(wb[e] << 16), acc);
-      acc = fmaf(__uint_as_float(wa[e] & 0xffff0000u), __uint_as_float(wb[e] & 0xffff0000u), acc);
+      for (int e = 0; e < 4; ++e) {
+        acc = fmaf(__uint_as_float(wa[e] << 16), __uint_as_float(wb[e] << 16), acc);
+        acc = fmaf(__uint_as_float(wa[e] & 0xffff0000u), __uint_as_float(wb[e] & 0xffff0000u), acc);
+      }
     }
+#pragma unroll
+    for (int w = kLanesPerRow / 2; w > 0; w >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, w);
+    if (row < rows && c == 0) delta[row] = acc;
+    // the accumulator rows r0 .. r0 + kRowsPerWarp - 1: D floats each, D / 4 float4
+    float4* z = reinterpret_cast<float4*>(dq_acc + r0 * D);
+    const long long n4 = (rows - r0 < kRowsPerWarp ? rows - r0 : kRowsPerWarp) * (D / 4);
+    for (long long i = lane; i < n4; i += 32) z[i] = make_float4(0.f, 0.f, 0.f, 0.f);
   }
-  delta[row] = acc;
 }
 
 // dQ (bf16) from the fp32 accumulation buffer.
@@ -609,13 +626,16 @@ fa_status launch(const void* q, const void* k, const void* v, const void* o, con
   using C = BwdCfg<D>;
   const uint64_t bh = static_cast<uint64_t>(B) * H;
   const long long rows = static_cast<long long>(bh) * N;
-  cudaError_t e = cudaMemsetAsync(dq_acc, 0, static_cast<size_t>(rows) * D * sizeof(float), stream);
-  if (e != cudaSuccess) {
-    set_error_text("cudaMemsetAsync(dQ accumulator)", e);
-    return FA_ERR_CUDA;
+  {
+    // enough warps for every row group, at most a few waves of the GPU
+    const long long groups = (rows + (32 / (D / 8)) - 1) / (32 / (D / 8));
+    const long long blocks = (groups + kPrepThreads / 32 - 1) / (kPrepThreads / 32);
+    const unsigned grid = static_cast<unsigned>(blocks < 152 * 16 ? blocks : 152 * 16);
+    bwd_prep_kernel<D><<<grid, kPrepThreads, 0, stream>>>(static_cast<const __nv_bfloat16*>(o),
+                                                          static_cast<const __nv_bfloat16*>(dout), delta, dq_acc,
+                                                          rows);
   }
-  bwd_delta_kernel<D><<<static_cast<unsigned>((rows + 255) / 256), 256, 0, stream>>>(
-      static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dout), delta, rows);
+  cudaError_t e = cudaSuccess;
   CUtensorMap tq, tk, tv, tdo, tdq;
   if (!encode_bf16_map(&tq, q, D, N, bh, 128) || !encode_bf16_map(&tk, k, D, N, bh, 128) ||
       !encode_bf16_map(&tv, v, D, N, bh, 128) || !encode_bf16_map(&tdo, dout, D, N, bh, 128) ||
