@@ -24,10 +24,11 @@
 //               so that S of the next tile runs while P/dS warps finish dS_i,
 //               and dP_{i+1} waits only for the read-out of dQ_i.
 //   warps 4-11  P and dS: warp w takes key rows 32(w%4).. and query columns
-//               64((w-4)/4)..; P = exp2(S log2e scale - L log2e) (kept in fp32
-//               registers), bf16 P^T to TMEM (for dV), then dS = P (dP - D) to
-//               TMEM (for dK) and, transposed, to shared memory (for dQ = dS K,
-//               whose A operand must be query-major).
+//               64((w-4)/4)..; P = exp2(S log2e scale - L log2e) rounded to bf16
+//               pairs, to TMEM (for dV) and kept in registers, then
+//               dS = P (dP - D) from those bf16 P values to TMEM (for dK) and,
+//               transposed, to shared memory (for dQ = dS K, whose A operand
+//               must be query-major).
 //   warps 0-3   read the dQ share out of TMEM and add scale * dQ to the fp32
 //               accumulator (the atomic additions of §7.4). d = 128: the share
 //               is dQ^T (d on the lanes); each warp loads three 32-column
@@ -370,8 +371,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         break;
       }
       tc_fence_after();
-      // P^T for this row and 64 queries, fp32 in registers
-      float pf[64];
+      // P^T for this row and 64 queries, 32 at a time, as bf16 pairs: to TMEM for
+      // dV, and kept for dS (32 registers)
+      uint32_t pw[32];
       const float4* l4 = reinterpret_cast<const float4*>(vec_l + b * 128 + 64 * half);
 #pragma unroll
       for (int h2 = 0; h2 < 2; ++h2) {
@@ -388,27 +390,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           f2_unpack(a, x0, x1);
           f2_unpack(c, x2, x3);
           const int e = 32 * h2 + 4 * e4;
-          pf[e] = ex2_approx(x0);
-          pf[e + 1] = ex2_approx(x1);
-          pf[e + 2] = ex2_approx(x2);
-          pf[e + 3] = ex2_approx(x3);
+          float p4[4] = {ex2_approx(x0), ex2_approx(x1), ex2_approx(x2), ex2_approx(x3)};
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            // no key beyond N; on the diagonal tile query 64 half + e + u sees this key only if not earlier
+            if (!key_ok || (p.causal && i == j && row > 64 * half + e + u)) p4[u] = 0.f;
+          }
+          pw[e / 2] = pack_bf16x2(p4[0], p4[1]);
+          pw[e / 2 + 1] = pack_bf16x2(p4[2], p4[3]);
         }
       }
-      if (!key_ok) {
-#pragma unroll
-        for (int e = 0; e < 64; ++e) pf[e] = 0.f;
-      } else if (p.causal && i == j) {
-        // the diagonal tile: query 64 half + e sees this key only if it is not earlier
-#pragma unroll
-        for (int e = 0; e < 64; ++e)
-          if (row > 64 * half + e) pf[e] = 0.f;
-      }
-      {
-        uint32_t pw[32];
-#pragma unroll
-        for (int e = 0; e < 32; ++e) pw[e] = pack_bf16x2(pf[2 * e], pf[2 * e + 1]);
-        tmem_st_x32(s_tm, pw);
-      }
+      tmem_st_x32(s_tm, pw);
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
@@ -439,10 +431,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         for (int e4 = 0; e4 < 8; ++e4) {
           const float4 dl = d4[8 * c + e4];
           const int e = 32 * c + 4 * e4;
-          const uint64_t a = f2_mul(f2_pack(pf[e], pf[e + 1]),
+          const uint32_t p01 = pw[e / 2], p23 = pw[e / 2 + 1];
+          const uint64_t a = f2_mul(f2_pack(__uint_as_float(p01 << 16), __uint_as_float(p01 & 0xffff0000u)),
                                     f2_add(f2_pack(__uint_as_float(dp[4 * e4]), __uint_as_float(dp[4 * e4 + 1])),
                                            f2_pack(-dl.x, -dl.y)));
-          const uint64_t q = f2_mul(f2_pack(pf[e + 2], pf[e + 3]),
+          const uint64_t q = f2_mul(f2_pack(__uint_as_float(p23 << 16), __uint_as_float(p23 & 0xffff0000u)),
                                     f2_add(f2_pack(__uint_as_float(dp[4 * e4 + 2]), __uint_as_float(dp[4 * e4 + 3])),
                                            f2_pack(-dl.z, -dl.w)));
           float x0, x1, x2, x3;
