@@ -671,7 +671,7 @@ def run_gpu(args, world, rank, local):
         perfmodel.decode_kv_bytes(gc.Hq, gc.d, gsl.tolist()) + gqa_kv
     leg_roofs = {
         "backward": leg_roof("tensor", bwd_value / world, peaks["bf16_tflops"], "TFLOP/s",
-                             "bwd_kernel_128_llama3_8b_prefill", "bwd_kernel<128> (+ delta, convert)",
+                             "bwd_kernel_128_llama3_8b_prefill", "bwd_kernel<128> (+ prep, convert)",
                              "burst " + tag),
         "fwd_fp8": leg_roof("tensor", fp8_value / world, 2 * peaks["bf16_tflops"], "TFLOP/s",
                             "fwd_kernel_128_fp8_llama3_8b_prefill", "fwd_kernel<128, e4m3>",
