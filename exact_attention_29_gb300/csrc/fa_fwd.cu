@@ -24,7 +24,10 @@
 //     (thread r of a warpgroup owns row r; a row's max and sum are in-thread);
 //   * warp 8: one thread issues every tcgen05.mma and commit;
 //   * warp 9: one thread issues every TMA copy (Q, then K_j, V_j into a ring
-//     of shared-memory slots).
+//     of shared-memory slots);
+//   * the epilogue of a tile stages O in 64-column boxes in shared memory and
+//     one of its threads stores each box with a TMA tensor store, so the O
+//     rows leave through the TMA unit rather than the load/store path.
 //   TMEM columns: S0 [0,128), S1 [128,256), O0 [256,256+D), O1 [256+D,256+2D).
 //   P (bf16 pairs) overwrites the first 64 columns of its S tile and is the
 //   TMEM A operand of O += P V. While warpgroup 0 runs the softmax of S0 the
@@ -83,7 +86,10 @@ struct Cfg {
   __host__ __device__ static constexpr uint32_t o_col(int t) { return t ? 256u + D : 256u; }
   static constexpr uint32_t kTmemCols = 512;
   static constexpr int kRingOff = 2 * kTileBytes;
-  static constexpr int kBarOff = kRingOff + kStages * kTileBytes;
+  // epilogue staging: per tile one 64-column box of O (128 rows x 128 bytes, 128-byte swizzle)
+  static constexpr int kOStageOff = kRingOff + kStages * kTileBytes;
+  static constexpr int kOStageBytes = 128 * 128;
+  static constexpr int kBarOff = kOStageOff + 2 * kOStageBytes;
   // q_full, q_empty, s_full, p_full, o_full, o_empty (2 each), kv_full, kv_empty, mma_done,
   // item_full, item_empty
   static constexpr int kNumBars = 12 + 2 * kStages + 1 + 2 * kItemSlots;
@@ -115,7 +121,6 @@ struct FwdParams {
   int num_pairs;   // Q-tile pairs per head
   int num_items;   // BH * num_pairs
   int causal;
-  int o_v8;          // o is 32-byte aligned: the epilogue writes 32-byte pieces of a row
   int swap_tiles;    // dense causal items: tile 0 takes the pair's second 128 rows
   float scale_log2;  // scale * log2(e)
 };
@@ -123,6 +128,7 @@ struct FwdParams {
 struct Smem {
   uint8_t* q[2];
   uint8_t* ring;
+  uint8_t* ostage;  // [2][kOStageBytes]
   uint64_t* q_full;    // [2]   Q tile landed
   uint64_t* q_empty;   // [2]   last S = Q K^T of an item done: Q buffer free (softmax arrives)
   uint64_t* s_full;    // [2]   S = Q K^T done (also: every earlier product done)
@@ -149,6 +155,7 @@ __device__ __forceinline__ Smem carve(uint8_t* raw) {
   s.q[0] = base;
   s.q[1] = base + C::kTileBytes;
   s.ring = base + C::kRingOff;
+  s.ostage = base + C::kOStageOff;
   uint64_t* bars = reinterpret_cast<uint64_t*>(base + C::kBarOff);
   s.q_full = bars;
   s.q_empty = bars + 2;
@@ -581,7 +588,8 @@ __device__ __forceinline__ void release_after_s(const Smem& sm, const Item& it, 
 
 // ---------------------------------------------------------------- softmax + epilogue (128 threads per tile)
 template <int D, bool F8, bool SP>
-__device__ void softmax_role(const Smem& sm, uint32_t tmem, const FwdParams& p, int warp, int lane) {
+__device__ void softmax_role(const Smem& sm, uint32_t tmem, const FwdParams& p, int warp, int lane,
+                             const CUtensorMap* tm_o) {
   using C = Cfg<D, F8>;
   const int t = warp >> 2;
   const int quarter = warp & 3;  // this warp may touch TMEM lanes [32*quarter, 32*quarter+32)
@@ -812,7 +820,9 @@ __device__ void softmax_role(const Smem& sm, uint32_t tmem, const FwdParams& p, 
     if (!ok) break;
     ok = bounded_wait(&sm.o_full[t], o_cnt & 1, sm.abort_flag, p.err, kSiteOFull);
     ++o_cnt;
-    ok = __all_sync(kFull, ok);
+    // one decision for the whole warpgroup: the epilogue below synchronises its
+    // 128 threads on named barriers, which every one of them must reach
+    ok = named_bar_and(1 + t, 128, ok);
     if (!ok) break;
     // the last P V of this tile is done: its V tile is free if this tile was its last reader
     // (block-sparse: every V is released by the issuing thread)
@@ -839,20 +849,30 @@ __device__ void softmax_role(const Smem& sm, uint32_t tmem, const FwdParams& p, 
     }
     tc_fence_before();
     mbar_arrive(&sm.o_empty[t]);
-    if (q_row < p.N) {
-      __nv_bfloat16* dst = p.o + (static_cast<size_t>(it.bh) * p.N + q_row) * D;
-      if (p.o_v8) {
-        // whole 32-byte sectors per lane: half the store instructions
+    // O leaves through the TMA unit: the warpgroup stages each 64-column box in
+    // the 128-byte swizzle of the map, and one thread stores it (rows beyond N
+    // are outside the map and not written)
+    uint8_t* ost = sm.ostage + t * C::kOStageBytes;
+    uint4* rowp = reinterpret_cast<uint4*>(ost + row * 128);
 #pragma unroll
-        for (int i = 0; i < D / 16; ++i) st_global_v8(dst + 16 * i, &w[8 * i]);
-      } else {
-        uint4* dst4 = reinterpret_cast<uint4*>(dst);
+    for (int c = 0; c < D / 64; ++c) {
+      if (releaser) bulk_wait_group_read<0>();  // the previous store has read the staging box
+      named_bar_sync(1 + t, 128);
 #pragma unroll
-        for (int i = 0; i < D / 8; ++i) dst4[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+      for (int u = 0; u < 8; ++u)
+        rowp[u ^ (row & 7)] = make_uint4(w[32 * c + 4 * u], w[32 * c + 4 * u + 1], w[32 * c + 4 * u + 2],
+                                         w[32 * c + 4 * u + 3]);
+      fence_proxy_async_smem();
+      named_bar_sync(1 + t, 128);
+      if (releaser) {
+        tma_store_3d(tm_o, ost, 64 * c, it.row(t), it.bh);
+        bulk_commit_group();
       }
-      p.lse[static_cast<size_t>(it.bh) * p.N + q_row] = (l > 0.f) ? (m_used + log2f(l)) * kLn2 : -INFINITY;
     }
+    if (q_row < p.N)
+      p.lse[static_cast<size_t>(it.bh) * p.N + q_row] = (l > 0.f) ? (m_used + log2f(l)) * kLn2 : -INFINITY;
   }
+  if (releaser) bulk_wait_group<0>();  // every O store complete before the CTA can exit
 #ifdef FA_DEBUG
   if (releaser) {
     sm.dbg[10 + t] = ring_next;
@@ -901,7 +921,7 @@ __global__ void __launch_bounds__(32) sparse_list_kernel(const uint8_t* __restri
 template <int D, bool F8, bool SP>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-               const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
+               const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o, const FwdParams p) {
   using C = Cfg<D, F8>;
   extern __shared__ uint8_t smem_raw[];
   const Smem sm = carve<D, F8>(smem_raw);
@@ -949,7 +969,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_role<D, F8, SP>(sm, tmem, p);
     }
   } else {
-    softmax_role<D, F8, SP>(sm, tmem, p, warp, lane);
+    softmax_role<D, F8, SP>(sm, tmem, p, warp, lane, &tm_o);
   }
 
   tc_fence_before();
@@ -974,7 +994,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 template <int D, bool F8, bool SP>
-fa_status launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, FwdParams prm, int B, int H,
+fa_status launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& to,
+                 FwdParams prm, int B, int H,
                  int N, int causal, float scale, cudaStream_t stream, int num_sms) {
   using C = Cfg<D, F8>;
   const uint64_t bh = static_cast<uint64_t>(B) * H;
@@ -985,7 +1006,6 @@ fa_status launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap
   prm.num_pairs = num_pairs;
   prm.num_items = static_cast<int>(items);
   prm.causal = causal ? 1 : 0;
-  prm.o_v8 = (reinterpret_cast<uintptr_t>(prm.o) & 31u) == 0 ? 1 : 0;
   // Which tile of a causal pair goes first is a matter of how the two tiles'
   // chains overlap at item boundaries; measured per instance: the swapped order
   // is faster for e4m3 (+2 %) and d = 64 (+6 %), slower for bf16 d = 128 (-1 to -3 %).
@@ -1000,7 +1020,7 @@ fa_status launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap
     return FA_ERR_CUDA;
   }
   const int grid = static_cast<int>(items < num_sms ? items : num_sms);
-  fwd_kernel<D, F8, SP><<<grid, kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, prm);
+  fwd_kernel<D, F8, SP><<<grid, kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, to, prm);
   e = cudaGetLastError();
   if (e != cudaSuccess) {
     set_error_text("fwd_kernel launch", e);
@@ -1014,10 +1034,10 @@ fa_status launch_bf16(const void* q, const void* k, const void* v, void* o, floa
                       int causal, float scale, cudaStream_t stream, unsigned int* err, int num_sms,
                       const uint32_t* list = nullptr, const int* cnt = nullptr, int mask_heads = 0,
                       int* next_item = nullptr) {
-  CUtensorMap tq, tk, tv;
+  CUtensorMap tq, tk, tv, to;
   const uint64_t bh = static_cast<uint64_t>(B) * H;
   if (!encode_bf16_map(&tq, q, D, N, bh, kBM) || !encode_bf16_map(&tk, k, D, N, bh, kBN) ||
-      !encode_bf16_map(&tv, v, D, N, bh, kBN))
+      !encode_bf16_map(&tv, v, D, N, bh, kBN) || !encode_bf16_map(&to, o, D, N, bh, kBM))
     return FA_ERR_CUDA;
   FwdParams prm{};
   prm.o = static_cast<__nv_bfloat16*>(o);
@@ -1027,8 +1047,8 @@ fa_status launch_bf16(const void* q, const void* k, const void* v, void* o, floa
   prm.cnt = cnt;
   prm.next_item = next_item;
   prm.mask_heads = mask_heads;
-  if (list != nullptr) return launch<D, false, true>(tq, tk, tv, prm, B, H, N, causal, scale, stream, num_sms);
-  return launch<D, false, false>(tq, tk, tv, prm, B, H, N, causal, scale, stream, num_sms);
+  if (list != nullptr) return launch<D, false, true>(tq, tk, tv, to, prm, B, H, N, causal, scale, stream, num_sms);
+  return launch<D, false, false>(tq, tk, tv, to, prm, B, H, N, causal, scale, stream, num_sms);
 }
 
 }  // namespace
@@ -1065,8 +1085,9 @@ fa_status launch_fwd_fp8(const void* q8, const void* k8, const void* vt8, const 
                          const float* v_scale, void* o, float* lse, int B, int H, int N, int d, int causal,
                          float scale, int v_pitch, cudaStream_t stream, unsigned int* err, int num_sms) {
   if (d != 128) return FA_ERR_UNSUPPORTED;
-  CUtensorMap tq, tk, tv;
+  CUtensorMap tq, tk, tv, to;
   const uint64_t bh = static_cast<uint64_t>(B) * H;
+  if (!encode_bf16_map(&to, o, 128, N, bh, kBM)) return FA_ERR_CUDA;
   // Q, K: [BH][N][128] bytes; V^T: [BH][128][v_pitch] bytes, keys inner
   if (!encode_u8_map(&tq, q8, 128, N, bh, kBM, 128) || !encode_u8_map(&tk, k8, 128, N, bh, kBN, 128) ||
       !encode_u8_map(&tv, vt8, N, 128, bh, 128, static_cast<uint64_t>(v_pitch)))
@@ -1078,7 +1099,7 @@ fa_status launch_fwd_fp8(const void* q8, const void* k8, const void* vt8, const 
   prm.sq = q_scale;
   prm.sk = k_scale;
   prm.sv = v_scale;
-  return launch<128, true, false>(tq, tk, tv, prm, B, H, N, causal, scale, stream, num_sms);
+  return launch<128, true, false>(tq, tk, tv, to, prm, B, H, N, causal, scale, stream, num_sms);
 }
 
 }  // namespace fa
