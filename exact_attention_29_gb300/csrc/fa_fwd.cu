@@ -93,7 +93,8 @@ struct Cfg {
   // q_full, q_empty, s_full, p_full, o_full, o_empty (2 each), kv_full, kv_empty, mma_done,
   // item_full, item_empty
   static constexpr int kNumBars = 12 + 2 * kStages + 1 + 2 * kItemSlots;
-  // + TMEM slot, abort flag, 16 protocol counters (FA_DEBUG), item slots, slack to align to 1 KB
+  // + TMEM slot, abort flag, output-map address, 16 protocol counters (FA_DEBUG), item slots,
+  // slack to align to 1 KB
   static constexpr int kSmemBytes = kBarOff + kNumBars * 8 + 16 + 64 + 4 * kItemSlots + 1024;
 };
 
@@ -144,6 +145,9 @@ struct Smem {
   volatile int* abort_flag;
   uint32_t* dbg;       // [16] per-role protocol counters, compared at the end (FA_DEBUG builds)
   volatile int* item_q;  // [kItemSlots] block-sparse: published item indices
+  // the generic address of the output tensor map (a kernel parameter), read by
+  // the epilogue's storing threads only: a register the softmax loop does not hold
+  const CUtensorMap* const* tmo;
 };
 
 template <int D, bool F8>
@@ -170,6 +174,7 @@ __device__ __forceinline__ Smem carve(uint8_t* raw) {
   s.item_empty = s.item_full + kItemSlots;
   s.tmem_slot = reinterpret_cast<uint32_t*>(s.item_empty + kItemSlots);
   s.abort_flag = reinterpret_cast<volatile int*>(s.tmem_slot + 1);
+  s.tmo = reinterpret_cast<const CUtensorMap* const*>(s.tmem_slot + 2);
   s.dbg = reinterpret_cast<uint32_t*>(s.tmem_slot + 4);
   s.item_q = reinterpret_cast<volatile int*>(s.dbg + 16);
   return s;
@@ -588,8 +593,7 @@ __device__ __forceinline__ void release_after_s(const Smem& sm, const Item& it, 
 
 // ---------------------------------------------------------------- softmax + epilogue (128 threads per tile)
 template <int D, bool F8, bool SP>
-__device__ void softmax_role(const Smem& sm, uint32_t tmem, const FwdParams& p, int warp, int lane,
-                             const CUtensorMap* tm_o) {
+__device__ void softmax_role(const Smem& sm, uint32_t tmem, const FwdParams& p, int warp, int lane) {
   using C = Cfg<D, F8>;
   const int t = warp >> 2;
   const int quarter = warp & 3;  // this warp may touch TMEM lanes [32*quarter, 32*quarter+32)
@@ -820,6 +824,9 @@ __device__ void softmax_role(const Smem& sm, uint32_t tmem, const FwdParams& p, 
     if (!ok) break;
     ok = bounded_wait(&sm.o_full[t], o_cnt & 1, sm.abort_flag, p.err, kSiteOFull);
     ++o_cnt;
+    // the staging box is free once this tile's previous TMA store has read it;
+    // the barrier below publishes that to the warpgroup
+    if (releaser) bulk_wait_group_read<0>();
     // one decision for the whole warpgroup: the epilogue below synchronises its
     // 128 threads on named barriers, which every one of them must reach
     ok = named_bar_and(1 + t, 128, ok);
@@ -835,37 +842,50 @@ __device__ void softmax_role(const Smem& sm, uint32_t tmem, const FwdParams& p, 
     // (a row that saw no key, possible under a block mask: o = 0, lse = -inf)
     const float inv_l = (l > 0.f) ? (F8 ? __ldg(p.sv + it.bh) : 1.f) / l : 0.f;
     const uint64_t inv_l2 = f2_pack(inv_l, inv_l);
-    uint32_t w[D / 2];
+    // O leaves through the TMA unit in 64-column boxes, staged in shared memory
+    // in the 128-byte swizzle of the map (16-byte chunk u of a row at u ^ (row & 7));
+    // one thread stores each box, and rows beyond N are outside the map.
+    // Columns [0, 64) go straight to the box; the rest wait in registers until
+    // the first box has been read.
+    uint4* rowp = reinterpret_cast<uint4*>(sm.ostage + t * C::kOStageBytes + row * 128);
+    uint32_t w[D > 64 ? (D - 64) / 2 : 1];
 #pragma unroll
     for (int c = 0; c < D; c += 32) {
       uint32_t r[32];
       tmem_ld_x32(o_tm + c, r);
+      uint32_t h[16];
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
         float lo, hi;
         f2_unpack(f2_mul(f2_pack(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1])), inv_l2), lo, hi);
-        w[c / 2 + i] = pack_bf16x2(lo, hi);
+        h[i] = pack_bf16x2(lo, hi);
+      }
+      if (c < 64) {
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          rowp[(c / 8 + u) ^ (row & 7)] = make_uint4(h[4 * u], h[4 * u + 1], h[4 * u + 2], h[4 * u + 3]);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) w[(c - 64) / 2 + i] = h[i];
       }
     }
     tc_fence_before();
     mbar_arrive(&sm.o_empty[t]);
-    // O leaves through the TMA unit: the warpgroup stages each 64-column box in
-    // the 128-byte swizzle of the map, and one thread stores it (rows beyond N
-    // are outside the map and not written)
     uint8_t* ost = sm.ostage + t * C::kOStageBytes;
-    uint4* rowp = reinterpret_cast<uint4*>(ost + row * 128);
 #pragma unroll
     for (int c = 0; c < D / 64; ++c) {
-      if (releaser) bulk_wait_group_read<0>();  // the previous store has read the staging box
-      named_bar_sync(1 + t, 128);
+      if (c > 0) {
+        if (releaser) bulk_wait_group_read<0>();  // the previous box has been read
+        named_bar_sync(1 + t, 128);
 #pragma unroll
-      for (int u = 0; u < 8; ++u)
-        rowp[u ^ (row & 7)] = make_uint4(w[32 * c + 4 * u], w[32 * c + 4 * u + 1], w[32 * c + 4 * u + 2],
-                                         w[32 * c + 4 * u + 3]);
+        for (int u = 0; u < 8; ++u)
+          rowp[u ^ (row & 7)] = make_uint4(w[32 * (c - 1) + 4 * u], w[32 * (c - 1) + 4 * u + 1],
+                                           w[32 * (c - 1) + 4 * u + 2], w[32 * (c - 1) + 4 * u + 3]);
+      }
       fence_proxy_async_smem();
       named_bar_sync(1 + t, 128);
       if (releaser) {
-        tma_store_3d(tm_o, ost, 64 * c, it.row(t), it.bh);
+        tma_store_3d(*sm.tmo, ost, 64 * c, it.row(t), it.bh);
         bulk_commit_group();
       }
     }
@@ -947,6 +967,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&sm.item_empty[e], kItemReaders);
     }
     *sm.abort_flag = 0;
+    *const_cast<const CUtensorMap**>(sm.tmo) = &tm_o;
     for (int i = 0; i < 16; ++i) sm.dbg[i] = 0;
     fence_barrier_init();
   }
@@ -969,7 +990,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_role<D, F8, SP>(sm, tmem, p);
     }
   } else {
-    softmax_role<D, F8, SP>(sm, tmem, p, warp, lane, &tm_o);
+    softmax_role<D, F8, SP>(sm, tmem, p, warp, lane);
   }
 
   tc_fence_before();
