@@ -33,6 +33,13 @@ def main(out_path):
         T = (N + 127) // 128
         mask = (torch.rand((3, T, T), generator=torch.Generator().manual_seed(N)) < 0.5).to(torch.uint8).cuda()
         keep(f"sparse_{N}_{d}_{int(causal)}", *fa.fa_fwd_sparse(q, k, v, mask, causal=causal))
+    # backward over several waves of CTAs (80 heads x 6 K/V tiles)
+    for d, causal in ((128, True), (64, False)):
+        q, k, v = wl.prefill_inputs(4, 20, 700, d, seed=d + 2, device="cuda")
+        dout = wl.backward_inputs(4, 20, 700, d, seed=d + 2, device="cuda")
+        o, lse = fa.fa_fwd(q, k, v, causal=causal)
+        dq, dk, dv = fa.fa_bwd(q, k, v, o, lse, dout, causal=causal)
+        keep(f"bwd_items_{d}_{int(causal)}", dk, dv)
     # block-sparse over 32 tiles: band + global + random rows, some block rows
     # keeping everything and some nothing (uneven private runs within a pair)
     for d, causal in ((128, False), (64, True)):

@@ -29,14 +29,30 @@ def _grads(q, k, v, do, causal, scale=None):
 @pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("N", [1, 7, 128, 129, 255, 256, 300, 384])
 def test_small_shapes_full_oracle(N, d, causal):
-    """One K/V tile per CTA: a single row, partial tiles, ragged tails, and
-    several K/V tiles whose dQ shares meet in the atomic accumulation."""
+    """Fewer work items (K/V tiles of a head) than SMs, one per CTA: a single
+    row, partial tiles, ragged tails, and several K/V tiles whose dQ shares
+    meet in the atomic accumulation."""
     B, H = (2, 2) if N <= 256 else (1, 2)
     q, k, v = wl.prefill_inputs(B, H, N, d, seed=N + d)
     do = wl.backward_inputs(B, H, N, d, seed=N + d)
     got = _grads(q, k, v, do, causal)
     ref = oracle.attention_bwd(q, k, v, do, causal, d ** -0.5)
     compare_grads(got, ref, f"N={N} d={d} causal={causal}")
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("d", [64, 128])
+def test_several_waves_full_oracle(d, causal):
+    """60 heads x 6 K/V tiles = 360 CTAs, more than two waves of the 152 SMs,
+    every gradient element against the oracle: under the causal mask the CTAs
+    of a wave walk very different numbers of Q tiles, and the last tile is
+    ragged."""
+    B, H, N = 3, 20, 700
+    q, k, v = wl.prefill_inputs(B, H, N, d, seed=d + 1)
+    do = wl.backward_inputs(B, H, N, d, seed=d + 1)
+    got = _grads(q, k, v, do, causal)
+    ref = oracle.attention_bwd(q, k, v, do, causal, d ** -0.5)
+    compare_grads(got, ref, f"B={B} H={H} N={N} d={d} causal={causal}")
 
 
 def test_non_default_scale():
