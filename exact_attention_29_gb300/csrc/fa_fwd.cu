@@ -837,7 +837,7 @@ __device__ void softmax_role(const Smem& sm, uint32_t tmem, const FwdParams& p, 
       mbar_arrive(&sm.kv_empty[(ring_base + 2 * (nkv - 1) + 1) % C::kStages]);
     tc_fence_after();
 
-    // Epilogue: O / l to bf16 in registers, release O's TMEM columns, then store.
+    // Epilogue: O / l to bf16, O's TMEM columns released once read, then stored.
     // (e4m3 V: O carries V's per-head scale)
     // (a row that saw no key, possible under a block mask: o = 0, lse = -inf)
     const float inv_l = (l > 0.f) ? (F8 ? __ldg(p.sv + it.bh) : 1.f) / l : 0.f;
