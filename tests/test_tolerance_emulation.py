@@ -1,10 +1,15 @@
-"""Where the GPU tolerances of the quantized paths come from.
+"""Where the GPU tolerances come from.
 
-The e4m3 forward and the backward round intermediates that the fp64 oracle
-keeps exact. These CPU tests redo the kernels' roundings (and only those) on
-the GPU tests' own inputs, in numpy next to the oracle, and check that the
-bounds the GPU tests use leave the margin their docstrings state over the
-error those roundings alone produce. Nothing here runs the CUDA path.
+The bf16 forward, the e4m3 forward and the backward round intermediates that
+the fp64 oracle keeps exact. These CPU tests redo the kernels' roundings (and
+only those) on the GPU tests' own inputs, in numpy next to the oracle, and
+check that the bounds the GPU tests use leave the margin their docstrings state
+over the error those roundings alone produce. Nothing here runs the CUDA path.
+
+bf16 forward (cicada blog §5 and CMU 15-779 Lecture 5 notes §5.1): S in fp32,
+the stale running maximum of the conditional rescale (threshold 8 in log2
+units), P = 2^(x - m) in fp32 with l summing the fp32 values, P rounded to
+bf16 for the P V product, O rounded to bf16 at the end.
 
 e4m3 forward ("已有的几种大模型上下文支持情况" §4.4, FA-3's FP8 path): S from
 the e4m3 codes, keys in 128-key tiles with the kernel's stale running maximum
@@ -23,7 +28,7 @@ import pytest
 import oracle
 from oracle import fp8 as ofp8
 from exact_attention_29_gb300 import workloads as wl
-from parity import GRAD_ATOL, GRAD_MAX_REL, GRAD_MEAN_REL
+from parity import GRAD_ATOL, GRAD_MAX_REL, GRAD_MEAN_REL, MAX_ABS_LSE, MAX_ABS_O, MEAN_ABS_O
 from test_gpu_fp8 import FP8_MAX_ABS_LSE, FP8_MAX_ABS_O, FP8_MEAN_ABS_O, _oracle_inputs, _signs
 
 LOG2E = 1.4426950408889634
@@ -35,6 +40,69 @@ def bf16(x):
     b = np.ascontiguousarray(np.asarray(x, dtype=np.float32)).view(np.uint32).astype(np.uint64)
     r = ((b + 0x7FFF + ((b >> 16) & 1)) & 0xFFFF0000).astype(np.uint32)
     return r.view(np.float32).astype(np.float64)
+
+
+def _bf16_forward_emulated(q, k, v, causal, scale, round_p=True):
+    """One head, fp64 [N, d] inputs (bf16 values): the kernel's roundings
+    (round_p=False keeps P in fp32, to show what its rounding adds)."""
+    N = q.shape[0]
+    s_all = (q @ k.T).astype(np.float32)
+    sl2 = np.float32(scale * LOG2E)
+    o = np.zeros_like(q)
+    lse = np.zeros(N)
+    for i in range(N):
+        vis = i + 1 if causal else N
+        m_used, l, acc = -np.inf, np.float32(0.0), np.zeros(q.shape[1])
+        for j0 in range(0, vis, 128):
+            s = s_all[i, j0:min(j0 + 128, vis)]
+            m_tile = float(np.float32(s.max()) * sl2)  # the maximum of the raw scores, then scaled
+            if m_used != -np.inf and m_tile > m_used + 8.0:
+                alpha = np.float32(2.0 ** (m_used - m_tile))
+                l, acc, m_used = np.float32(l * alpha), acc * float(alpha), m_tile
+            if m_used == -np.inf:
+                m_used = m_tile
+            p = np.exp2((s * sl2 - np.float32(m_used)).astype(np.float32), dtype=np.float32)
+            l = np.float32(l + p.sum(dtype=np.float32))
+            acc += (bf16(p) if round_p else p.astype(np.float64)) @ v[j0:j0 + p.size]
+        o[i] = acc / float(l)
+        lse[i] = (m_used + np.log2(float(l))) * LN2
+    return bf16(o), lse
+
+
+def test_bf16_forward_bounds_cover_the_roundings():
+    """The forward tests' shapes and criterion (max and mean of |dO| over the
+    whole output, max |dLSE|): the bounds over the rounding-only error. Measured
+    here: max |dO| up to 8.5e-3 (d = 64, 128 keys, causal) and mean |dO| up to
+    7.3e-4 (7 keys per row), so the max bound is 2.35x and the mean bound 2.74x
+    the rounding-only error at their worst; the LSE sums fp32 values and its
+    error stays near 3e-7, thousands of times below its bound. The maximum is
+    set mostly by the bf16 rounding of O itself (7.8e-3 with P in fp32: half a
+    bf16 step at |o| in [4, 8)); rounding P raises the mean by about a sixth."""
+    worst_max = worst_mean = worst_lse = worst_mean_fp32_p = 0.0
+    for d in (64, 128):
+        for N in (1, 7, 128, 129, 300, 1000):
+            for causal in (False, True):
+                B, H = (2, 2) if N <= 300 else (1, 2)
+                q, k, v = wl.prefill_inputs(B, H, N, d, seed=N + d)
+                o_ref, lse_ref = oracle.attention(q, k, v, causal, d ** -0.5)
+                qq, kk, vv = (t.double().numpy() for t in (q, k, v))
+                o, lse = np.zeros_like(o_ref), np.zeros_like(lse_ref)
+                o32 = np.zeros_like(o_ref)
+                for b in range(B):
+                    for h in range(H):
+                        o[b, h], lse[b, h] = _bf16_forward_emulated(qq[b, h], kk[b, h], vv[b, h], causal, d ** -0.5)
+                        o32[b, h] = _bf16_forward_emulated(qq[b, h], kk[b, h], vv[b, h], causal, d ** -0.5,
+                                                           round_p=False)[0]
+                worst_mean_fp32_p = max(worst_mean_fp32_p, np.abs(o32 - o_ref).mean())
+                do = np.abs(o - o_ref)
+                worst_max = max(worst_max, do.max())
+                worst_mean = max(worst_mean, do.mean())
+                worst_lse = max(worst_lse, np.abs(lse - lse_ref).max())
+    assert MAX_ABS_O / worst_max >= 2.2, worst_max
+    assert MEAN_ABS_O / worst_mean >= 2.5, worst_mean
+    assert MAX_ABS_LSE / worst_lse >= 100, worst_lse
+    # the emulation rounds P: its bf16 rounding adds to the error of the bf16 output alone
+    assert worst_mean > 1.1 * worst_mean_fp32_p, (worst_mean, worst_mean_fp32_p)
 
 
 def _fp8_forward_emulated(qd, kd, vd, causal, scale):
